@@ -1,0 +1,195 @@
+"""FP64 CPU oracle for paged attention over an FP8 E4M3 KV cache.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may use this package; the library never does.
+
+The computation lives in ``fp8kv_oracle.cpp`` (plain C++17, double precision,
+``std::thread`` over query rows).  This module compiles it with g++ and wraps
+it with ctypes.  Inputs are ``synth.Problem`` objects (CPU tensors).
+
+Parity status of each exported function (what pins it, in ``tests/``):
+  e4m3 table          format definition closed form + torch float8_e4m3fn
+  fp16 decode         all 65536 codes against numpy float16
+  attention           exact-rational evaluation on tiny inputs, closed forms
+                      (single token, constant keys, two tokens), invariants
+                      (page permutation, split count, sparse order/padding,
+                      all-visible sparse == dense causal), planted mistakes
+  attention_split     equals attention within 1e-13 (split-count invariance)
+  row_weights         sum to 1, two-token logistic closed form
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8kv_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+
+CXXFLAGS = ["-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            "-pthread", "-Wall"]
+
+
+def lib_path(plant: int = 0) -> str:
+    name = "liboracle.so" if plant == 0 else f"liboracle_plant{plant}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(plant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (plant != 0 builds a deliberately broken variant)."""
+    out = lib_path(plant)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", *CXXFLAGS, f"-DORC_PLANT={plant}", "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class OrcProblem(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_int), ("B", ctypes.c_int), ("q", ctypes.c_int),
+        ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
+        ("page_size", ctypes.c_int),
+        ("q_bits", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("k_stride", ctypes.c_int64 * 3), ("v_stride", ctypes.c_int64 * 3),
+        ("block_table", ctypes.c_void_p), ("bt_stride", ctypes.c_int64),
+        ("row_len", ctypes.c_void_p),
+        ("entry_tbl", ctypes.c_void_p), ("entry_mask", ctypes.c_void_p),
+        ("n_entries", ctypes.c_void_p), ("entry_stride", ctypes.c_int64),
+        ("softmax_scale", ctypes.c_double), ("k_scale", ctypes.c_double),
+        ("v_scale", ctypes.c_double),
+    ]
+
+
+_libs = {}
+
+
+def load(plant: int = 0) -> ctypes.CDLL:
+    if plant in _libs:
+        return _libs[plant]
+    path = build(plant)
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(OrcProblem)
+    lib.orc_e4m3.restype = ctypes.c_double
+    lib.orc_e4m3.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_table.argtypes = [ctypes.c_void_p]
+    lib.orc_f16.restype = ctypes.c_double
+    lib.orc_f16.argtypes = [ctypes.c_uint16]
+    lib.orc_attention.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_attention_items.argtypes = [P, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_attention_split.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_row_weights.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    _libs[plant] = lib
+    return lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+class _Pinned:
+    """Keeps the CPU tensors referenced by an OrcProblem alive."""
+
+    def __init__(self, p, k_cache=None, v_cache=None, row_len=None):
+        kc = p.k_cache if k_cache is None else k_cache
+        vc = p.v_cache if v_cache is None else v_cache
+        for t in (kc, vc):
+            assert t.device.type == "cpu" and t.dtype == torch.uint8
+        self.keep = []
+        s = OrcProblem()
+        s.mode = 0 if p.mode == "dense" else 1
+        s.B, s.q, s.Hq, s.Hkv, s.D = p.B, p.q, p.Hq, p.Hkv, p.D
+        s.page_size = p.page_size
+        qb = p.q_fp16.contiguous().view(torch.int16)
+        self.keep.append(qb)
+        s.q_bits = qb.data_ptr()
+        s.k_cache = kc.data_ptr()
+        s.v_cache = vc.data_ptr()
+        ks, vs = kc.stride(), vc.stride()
+        s.k_stride[:] = [ks[0], ks[1], ks[2]]
+        s.v_stride[:] = [vs[0], vs[1], vs[2]]
+        self.keep += [kc, vc]
+        if p.mode == "dense":
+            bt = p.block_table.contiguous()
+            rl = (p.row_len if row_len is None else torch.as_tensor(row_len, dtype=torch.int32)).contiguous()
+            self.keep += [bt, rl]
+            s.block_table = bt.data_ptr()
+            s.bt_stride = bt.shape[1]
+            s.row_len = rl.data_ptr()
+        else:
+            et = p.entry_tbl.contiguous()
+            em = p.entry_mask.contiguous()
+            ne = p.n_entries.contiguous()
+            self.keep += [et, em, ne]
+            s.entry_tbl = et.data_ptr()
+            s.entry_mask = em.data_ptr()
+            s.n_entries = ne.data_ptr()
+            s.entry_stride = et.shape[1]
+        s.softmax_scale = p.softmax_scale
+        s.k_scale = p.k_scale
+        s.v_scale = p.v_scale
+        self.s = s
+
+
+def e4m3_table(plant: int = 0) -> np.ndarray:
+    out = np.zeros(256, dtype=np.float64)
+    load(plant).orc_e4m3_table(out.ctypes.data)
+    return out
+
+
+def f16_value(bits: int, plant: int = 0) -> float:
+    return load(plant).orc_f16(bits)
+
+
+def attention(p, threads: Optional[int] = None, plant: int = 0, **over) -> np.ndarray:
+    """Full output [B][q][Hq][D] in float64.  ``over`` may replace k_cache,
+    v_cache or row_len with other CPU tensors of the same layout."""
+    pin = _Pinned(p, **over)
+    out = np.zeros((p.B, p.q, p.Hq, p.D), dtype=np.float64)
+    rc = load(plant).orc_attention(ctypes.byref(pin.s), out.ctypes.data, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
+    return out
+
+
+def attention_items(p, items, threads: Optional[int] = None, plant: int = 0, **over) -> np.ndarray:
+    """Outputs of the listed (b, r, h) triples only: [n][D] float64."""
+    pin = _Pinned(p, **over)
+    it = np.ascontiguousarray(np.asarray(items, dtype=np.int32).reshape(-1, 3))
+    out = np.zeros((it.shape[0], p.D), dtype=np.float64)
+    rc = load(plant).orc_attention_items(ctypes.byref(pin.s), it.ctypes.data, it.shape[0],
+                                         out.ctypes.data, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the problem or an item")
+    return out
+
+
+def attention_split(p, num_splits: int, threads: Optional[int] = None, plant: int = 0, **over) -> np.ndarray:
+    pin = _Pinned(p, **over)
+    out = np.zeros((p.B, p.q, p.Hq, p.D), dtype=np.float64)
+    rc = load(plant).orc_attention_split(ctypes.byref(pin.s), num_splits, out.ctypes.data,
+                                         threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
+    return out
+
+
+def row_weights(p, b: int, r: int, h: int, plant: int = 0, **over) -> np.ndarray:
+    pin = _Pinned(p, **over)
+    cap = 1 << 22
+    buf = np.zeros(cap, dtype=np.float64)
+    n = load(plant).orc_row_weights(ctypes.byref(pin.s), b, r, h, buf.ctypes.data, cap)
+    return buf[:n].copy()

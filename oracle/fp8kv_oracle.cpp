@@ -1,0 +1,336 @@
+// FP64 CPU oracle for paged attention over an FP8 E4M3 KV cache.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the library (fp8_e4m3_paged_gb300)
+// may include, link or call this file; only the tests, the package smoke check
+// and the benchmark's CPU-baseline leg use it.  It shares no code, header,
+// table or constant with the CUDA path.
+//
+// What it computes is the plain definition of softmax attention over the
+// exactly decoded E4M3 cache contents, in double precision:
+//
+//   z_j   = softmax_scale * k_scale * sum_d q[d] * dec(K_j[d])
+//   w_j   = exp(z_j - max z) / sum_i exp(z_i - max z)
+//   out_d = v_scale * sum_j w_j * dec(V_j[d])
+//
+// over the tokens j that a query row may see.  Sources:
+//  * per-tensor scales fold into the logits and the output
+//    ("Qwen4Exp: fp8_e4m3 main KV cache on the QSA path", review thread:
+//    k_scale pre-multiplied into the softmax scale, v_scale as output scale;
+//    Changes: the kernel dequantises K/V and folds the K and V scales);
+//  * live per-query lengths, zero meaning a dead row
+//    ("DFlash2 E4M3 attention with FP32 state", intro paragraph 3);
+//  * runtime page stride / block table addressing (same page, paragraph 5;
+//    "Qualify calibrated E4M3 and disk PLE with QSA DCP2", commit on packed
+//    pages: kernels honour the block stride);
+//  * four-token microblocks with 32-bit per-row visibility masks, mask-0
+//    padding entries on the null block (same page, commit "grouped page4
+//    null-block padding").
+//  * the split-KV partition scheme (FP32 unnormalised numerators, separate
+//    max and sum, then a combine) of "DFlash2 E4M3 attention with FP32 state",
+//    intro paragraph 4 -- written here in FP64 as orc_attention_split.
+//
+// E4M3 is the OCP "E4M3FN" format: 1 sign, 4 exponent (bias 7), 3 mantissa
+// bits, no infinities, 0x7F/0xFF are NaN, largest finite magnitude 448.
+// The oracle reads only the bytes of visible tokens, so poisoned bytes of
+// padding or unused page slots never reach it.
+//
+// Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -shared -fPIC -pthread
+//
+// Parity pins: every function here is pinned by CPU tests (decode tables
+// against the format definition and torch's converters; attention against an
+// independent exact-rational evaluation on tiny inputs, closed forms and
+// invariants).
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+#include <algorithm>
+
+#define ORC_API extern "C"
+
+typedef struct {
+  int mode;  // 0 = dense paged, 1 = sparse four-token microblocks
+  int B, q, Hq, Hkv, D;
+  int page_size;                 // tokens per physical block (4 in sparse mode)
+  const uint16_t* q_bits;        // [B][q][Hq][D] IEEE binary16 bit patterns
+  const uint8_t* k_cache;        // E4M3 bytes
+  const uint8_t* v_cache;
+  int64_t k_stride[3];           // byte strides: block, token, head
+  int64_t v_stride[3];
+  const int32_t* block_table;    // dense: [B][bt_stride]
+  int64_t bt_stride;
+  const int32_t* row_len;        // dense: [B][q], 0 = dead row
+  const int32_t* entry_tbl;      // sparse: [B][entry_stride]
+  const uint32_t* entry_mask;    // sparse: [B][entry_stride]
+  const int32_t* n_entries;      // sparse: [B]
+  int64_t entry_stride;
+  double softmax_scale, k_scale, v_scale;
+} orc_problem;
+
+// ORC_PLANT (compile-time, default 0 = none) plants one plausible mistake;
+// only the test that checks that the pins catch such mistakes builds those
+// variants.
+#ifndef ORC_PLANT
+#define ORC_PLANT 0
+#endif
+
+// ---------------------------------------------------------------- decoders
+
+// E4M3 byte -> value, straight from the format definition.
+ORC_API double orc_e4m3(uint8_t b) {
+  const int s = b >> 7;
+  const int e = (b >> 3) & 15;
+  const int m = b & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  double v;
+  if (e == 0)
+    v = std::ldexp((double)m, -9);                 // m/8 * 2^(1-7)
+  else
+    v = std::ldexp(1.0 + (double)m / 8.0, e - 7);
+#if ORC_PLANT == 1
+  if (e == 0) v = std::ldexp((double)m, -10);  // planted: wrong subnormal exponent
+#endif
+  return s ? -v : v;
+}
+
+ORC_API void orc_e4m3_table(double* out256) {
+  for (int i = 0; i < 256; ++i) out256[i] = orc_e4m3((uint8_t)i);
+}
+
+// IEEE binary16 bits -> value.
+ORC_API double orc_f16(uint16_t h) {
+  const int s = h >> 15;
+  const int e = (h >> 10) & 31;
+  const int m = h & 1023;
+  double v;
+  if (e == 31)
+    v = m ? std::numeric_limits<double>::quiet_NaN() : std::numeric_limits<double>::infinity();
+  else if (e == 0)
+    v = std::ldexp((double)m, -24);
+  else
+    v = std::ldexp(1.0 + (double)m / 1024.0, e - 15);
+  return s ? -v : v;
+}
+
+// ------------------------------------------------------- visible token set
+
+struct Tok { int64_t k_off, v_off; };
+
+// Tokens query row r of request b sees, for KV head g, in sequence order.
+static void visible(const orc_problem* p, int b, int r, int g, std::vector<Tok>& out) {
+  out.clear();
+  if (p->mode == 0) {
+    int n = p->row_len[(int64_t)b * p->q + r];
+#if ORC_PLANT == 4
+    if (n > 0) n -= 1;  // planted: off-by-one causal limit
+#endif
+    for (int j = 0; j < n; ++j) {
+      const int64_t blk = p->block_table[(int64_t)b * p->bt_stride + j / p->page_size];
+      const int64_t slot = j % p->page_size;
+      out.push_back({blk * p->k_stride[0] + slot * p->k_stride[1] + (int64_t)g * p->k_stride[2],
+                     blk * p->v_stride[0] + slot * p->v_stride[1] + (int64_t)g * p->v_stride[2]});
+    }
+  } else {
+    const int ne = p->n_entries[b];
+    for (int e = 0; e < ne; ++e) {
+      const int64_t blk = p->entry_tbl[(int64_t)b * p->entry_stride + e];
+      const uint32_t msk = p->entry_mask[(int64_t)b * p->entry_stride + e];
+        for (int t = 0; t < 4; ++t) {
+#if ORC_PLANT == 6
+        if ((msk >> (8 * t + r)) & 1u) {  // planted: transposed mask bit layout
+#else
+        if ((msk >> (4 * r + t)) & 1u) {
+#endif
+          out.push_back({blk * p->k_stride[0] + (int64_t)t * p->k_stride[1] + (int64_t)g * p->k_stride[2],
+                         blk * p->v_stride[0] + (int64_t)t * p->v_stride[1] + (int64_t)g * p->v_stride[2]});
+        }
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------- one row-head
+
+// Logits of query (b, r, h) over its visible tokens.
+static void logits(const orc_problem* p, int b, int r, int h, const std::vector<Tok>& toks,
+                   std::vector<double>& z) {
+  const int D = p->D;
+  const uint16_t* qv = p->q_bits + (((int64_t)b * p->q + r) * p->Hq + h) * D;
+  std::vector<double> qd(D);
+  for (int d = 0; d < D; ++d) qd[d] = orc_f16(qv[d]);
+  z.resize(toks.size());
+  for (size_t j = 0; j < toks.size(); ++j) {
+    const uint8_t* kb = p->k_cache + toks[j].k_off;
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += qd[d] * orc_e4m3(kb[d]);
+    double sc = p->softmax_scale * p->k_scale;
+#if ORC_PLANT == 2
+    sc = p->softmax_scale;  // planted: k_scale dropped
+#endif
+    z[j] = sc * dot;
+  }
+}
+
+static int group_of(const orc_problem* p, int h) {
+  const int G = p->Hq / p->Hkv;
+#if ORC_PLANT == 3
+  return h % p->Hkv;  // planted: interleaved head grouping
+#endif
+  return h / G;
+}
+
+// Softmax weights of query (b, r, h); returns the visible count.
+ORC_API int orc_row_weights(const orc_problem* p, int b, int r, int h, double* w, int cap) {
+  std::vector<Tok> toks;
+  visible(p, b, r, group_of(p, h), toks);
+  std::vector<double> z;
+  logits(p, b, r, h, toks, z);
+  const int n = (int)toks.size();
+  if (n == 0) return 0;
+  double M = -std::numeric_limits<double>::infinity();
+  for (double v : z) M = std::max(M, v);
+  double S = 0.0;
+  for (double v : z) S += std::exp(v - M);
+  for (int j = 0; j < n && j < cap; ++j) w[j] = std::exp(z[j] - M) / S;
+  return n;
+}
+
+static void row_head(const orc_problem* p, int b, int r, int h, double* out) {
+  const int D = p->D;
+  std::vector<Tok> toks;
+  visible(p, b, r, group_of(p, h), toks);
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  if (toks.empty()) return;  // dead row: +0.0
+  std::vector<double> z;
+  logits(p, b, r, h, toks, z);
+  double M = -std::numeric_limits<double>::infinity();
+  for (double v : z) M = std::max(M, v);
+  double S = 0.0;
+  for (double v : z) S += std::exp(v - M);
+#if ORC_PLANT == 8
+  S = 1.0 + 0.0 * S;  // planted: weights left unnormalised
+#endif
+  std::vector<double> acc(D, 0.0);
+  for (size_t j = 0; j < toks.size(); ++j) {
+    const double w = std::exp(z[j] - M) / S;
+#if ORC_PLANT == 7
+    const uint8_t* vb = p->k_cache + toks[j].k_off;  // planted: K read in place of V
+#else
+    const uint8_t* vb = p->v_cache + toks[j].v_off;
+#endif
+    for (int d = 0; d < D; ++d) acc[d] += w * orc_e4m3(vb[d]);
+  }
+  double vs = p->v_scale;
+#if ORC_PLANT == 5
+  vs = 1.0;  // planted: v_scale dropped
+#endif
+  for (int d = 0; d < D; ++d) out[d] = vs * acc[d];
+}
+
+// Split-KV in FP64: the visible sequence is cut into num_splits contiguous
+// partitions; each stores an unnormalised numerator, its own max and its own
+// sum; the combine rescales every partition to the global max and divides by
+// the rescaled total.  Empty partitions hold (max=-inf, sum=0) and are skipped.
+static void row_head_split(const orc_problem* p, int b, int r, int h, int S_, double* out) {
+  const int D = p->D;
+  std::vector<Tok> toks;
+  visible(p, b, r, group_of(p, h), toks);
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  const int n = (int)toks.size();
+  if (n == 0) return;
+  std::vector<double> z;
+  logits(p, b, r, h, toks, z);
+  const int chunk = (n + S_ - 1) / S_;
+  std::vector<double> m(S_, -std::numeric_limits<double>::infinity()), l(S_, 0.0);
+  std::vector<double> num((size_t)S_ * D, 0.0);
+  for (int s = 0; s < S_; ++s) {
+    const int j0 = s * chunk, j1 = std::min(n, j0 + chunk);
+    for (int j = j0; j < j1; ++j) m[s] = std::max(m[s], z[j]);
+    for (int j = j0; j < j1; ++j) {
+      const double e = std::exp(z[j] - m[s]);
+      l[s] += e;
+      const uint8_t* vb = p->v_cache + toks[j].v_off;
+      for (int d = 0; d < D; ++d) num[(size_t)s * D + d] += e * orc_e4m3(vb[d]);
+    }
+  }
+  double M = -std::numeric_limits<double>::infinity();
+  for (int s = 0; s < S_; ++s) M = std::max(M, m[s]);
+  double L = 0.0;
+  std::vector<double> acc(D, 0.0);
+  for (int s = 0; s < S_; ++s) {
+    if (l[s] == 0.0) continue;
+    const double w = std::exp(m[s] - M);
+    L += w * l[s];
+    for (int d = 0; d < D; ++d) acc[d] += w * num[(size_t)s * D + d];
+  }
+  for (int d = 0; d < D; ++d) out[d] = p->v_scale * acc[d] / L;
+}
+
+// ------------------------------------------------------------- drivers
+
+static int check(const orc_problem* p) {
+  if (!p || p->B < 0 || p->q < 1 || p->Hq < 1 || p->Hkv < 1 || p->D < 1) return -1;
+  if (p->Hq % p->Hkv) return -1;
+  if (p->mode == 1 && p->q > 8) return -1;
+  return 0;
+}
+
+template <class F>
+static void parallel_items(int64_t n, int nthreads, F f) {
+  if (nthreads <= 1 || n < 2) {
+    for (int64_t i = 0; i < n; ++i) f(i);
+    return;
+  }
+  nthreads = (int)std::min<int64_t>(nthreads, n);
+  std::vector<std::thread> th;
+  for (int t = 0; t < nthreads; ++t)
+    th.emplace_back([=]() {
+      for (int64_t i = t; i < n; i += nthreads) f(i);
+    });
+  for (auto& x : th) x.join();
+}
+
+// out: [B][q][Hq][D] doubles.
+ORC_API int orc_attention(const orc_problem* p, double* out, int nthreads) {
+  if (check(p)) return -1;
+  const int64_t n = (int64_t)p->B * p->q * p->Hq;
+  parallel_items(n, nthreads, [&](int64_t i) {
+    const int h = (int)(i % p->Hq);
+    const int r = (int)((i / p->Hq) % p->q);
+    const int b = (int)(i / ((int64_t)p->Hq * p->q));
+    row_head(p, b, r, h, out + i * p->D);
+  });
+  return 0;
+}
+
+// Only the listed (b, r, h) triples; out: [n_items][D].
+ORC_API int orc_attention_items(const orc_problem* p, const int32_t* items, int n_items, double* out,
+                        int nthreads) {
+  if (check(p)) return -1;
+  for (int i = 0; i < n_items; ++i) {
+    const int b = items[3 * i], r = items[3 * i + 1], h = items[3 * i + 2];
+    if (b < 0 || b >= p->B || r < 0 || r >= p->q || h < 0 || h >= p->Hq) return -1;
+  }
+  parallel_items(n_items, nthreads, [&](int64_t i) {
+    row_head(p, items[3 * i], items[3 * i + 1], items[3 * i + 2], out + i * p->D);
+  });
+  return 0;
+}
+
+ORC_API int orc_attention_split(const orc_problem* p, int num_splits, double* out, int nthreads) {
+  if (check(p) || num_splits < 1) return -1;
+  const int64_t n = (int64_t)p->B * p->q * p->Hq;
+  parallel_items(n, nthreads, [&](int64_t i) {
+    const int h = (int)(i % p->Hq);
+    const int r = (int)((i / p->Hq) % p->q);
+    const int b = (int)(i / ((int64_t)p->Hq * p->q));
+    row_head_split(p, b, r, h, num_splits, out + i * p->D);
+  });
+  return 0;
+}
+
+ORC_API int orc_abi_version(void) { return 1; }
+

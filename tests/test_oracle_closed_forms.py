@@ -1,0 +1,94 @@
+"""Closed-form pins for the oracle.
+
+* one visible token: the weight is exactly 1, so out = v_scale * dec(v);
+* identical keys: uniform weights, so out = v_scale * mean(dec(V)) (an exact
+  rational, compared here with Fractions);
+* two tokens: w_1 = 1 / (1 + exp(z_2 - z_1)), the logistic function;
+* dead rows (live length 0, or a sparse row with no visible bit) are +0.0;
+* v_scale is a pure output factor; k_scale and softmax_scale enter only as a
+  product.
+"""
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from synth import make_dense, make_sparse
+
+
+def _dec(byte):
+    return float(torch.tensor([byte], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64))
+
+
+def test_single_token_exact(orc):
+    p = make_dense(B=1, q=2, Hq=2, Hkv=1, D=8, page_size=4, lens=[6], seed=11,
+                   row_len=[[1, 0]], value_mode="direct", k_scale=0.5, v_scale=1.9)
+    out = orc.attention(p)
+    blk = int(p.block_table[0, 0])
+    vbytes = p.v_cache[blk, 0, 0].tolist()
+    want = np.array([1.9 * _dec(b) for b in vbytes])
+    assert np.array_equal(out[0, 0, 0], want)
+    assert np.array_equal(out[0, 0, 1], want)
+    assert np.all(out[0, 1] == 0.0) and not np.signbit(out[0, 1]).any()
+
+
+def test_constant_keys_give_mean(orc):
+    p = make_dense(B=1, q=1, Hq=1, Hkv=1, D=16, page_size=5, lens=[13], seed=12)
+    # every token gets the same key bytes
+    k0 = p.k_cache[int(p.block_table[0, 0]), 0, 0].clone()
+    for j in range(13):
+        p.k_cache[int(p.block_table[0, j // 5]), j % 5, 0] = k0
+    out = orc.attention(p)[0, 0, 0]
+    vs = Fraction(p.v_scale)
+    for d in range(16):
+        vals = [Fraction(_dec(int(p.v_cache[int(p.block_table[0, j // 5]), j % 5, 0, d]))) for j in range(13)]
+        exact = vs * sum(vals) / 13
+        # a 13-term double sum: error bounded by a few ulps of sum |terms|
+        scale = vs * sum(abs(v) for v in vals) / 13
+        assert abs(Fraction(out[d]) - exact) <= scale * Fraction(1, 2**48)
+
+
+def test_two_tokens_logistic(orc):
+    p = make_dense(B=1, q=1, Hq=1, Hkv=1, D=4, page_size=2, lens=[2], seed=13, softmax_scale=0.3)
+    w = orc.row_weights(p, 0, 0, 0)
+    qv = p.q_fp16[0, 0, 0].double().numpy()
+    kz = []
+    for j in range(2):
+        kb = p.k_cache[int(p.block_table[0, 0]), j, 0]
+        kd = kb.view(torch.float8_e4m3fn).double().numpy()
+        kz.append(0.3 * p.k_scale * float(qv @ kd))
+    w1 = 1.0 / (1.0 + math.exp(kz[1] - kz[0]))
+    assert len(w) == 2
+    assert abs(w[0] - w1) < 1e-15 and abs(w[1] - (1 - w1)) < 1e-15
+
+
+def test_weights_sum_to_one(orc):
+    p = make_dense(B=1, q=4, Hq=2, Hkv=1, D=32, page_size=7, lens=[300], seed=14)
+    for r in range(4):
+        w = orc.row_weights(p, 0, r, 1)
+        assert len(w) == int(p.row_len[0, r])
+        assert abs(w.sum() - 1.0) < 1e-12 and (w > 0).all()
+
+
+def test_dead_sparse_row(orc):
+    p = make_sparse(B=1, q=3, Hq=3, Hkv=1, D=8, L=40, topk_blocks=2, seed=15)
+    p.entry_mask[:] = torch.where(p.entry_mask != 0, p.entry_mask & 0x0FF, p.entry_mask)  # row 2 sees nothing
+    out = orc.attention(p)
+    assert np.all(out[0, 2] == 0.0)
+    assert np.abs(out[0, 0]).sum() > 0
+
+
+def test_scale_roles(orc):
+    p = make_dense(B=1, q=2, Hq=2, Hkv=1, D=16, page_size=8, lens=[40], seed=16,
+                   value_mode="direct", k_scale=0.37, v_scale=1.9, softmax_scale=0.25)
+    a = orc.attention(p)
+    p2 = make_dense(B=1, q=2, Hq=2, Hkv=1, D=16, page_size=8, lens=[40], seed=16,
+                    value_mode="direct", k_scale=0.25, v_scale=3.8, softmax_scale=0.37)
+    b = orc.attention(p2)
+    np.testing.assert_allclose(b, 2.0 * a, rtol=1e-15, atol=0)
+    # k_scale changes the weights (not a pure output factor)
+    p3 = make_dense(B=1, q=2, Hq=2, Hkv=1, D=16, page_size=8, lens=[40], seed=16,
+                    value_mode="direct", k_scale=0.74, v_scale=1.9, softmax_scale=0.25)
+    assert np.abs(orc.attention(p3) - a).max() > 1e-3
