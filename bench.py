@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark: attended-KV GB/s of paged E4M3 attention (split + combine).
+
+One step = one pass of the whole path (plan made once; split kernel + combine
+kernel) over one batch of synthetic input: by default the verify workload
+q=8 rows, Hq=6/Hkv=1, D=256, 131072-token context in 1728-token pages.
+Inputs stay resident in HBM; several copies of the KV pool are rotated so
+that each step reads bytes the L2 no longer holds.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle
+instead, on bounded samples of the same workload.
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
+torchrun, each rank runs an independent replica (no collective on the data
+path) and the job's value is the sum of bytes over the max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import attended_kv_bytes, make_problem  # noqa: E402
+
+METRIC = "attended-KV GB/s and µs/step (q8 Hq6/Hkv1/D256 @128K ctx), % of HBM peak"
+WORKLOAD_DESC = {
+    "c3_128k": "verify q=8 rows, Hq=6/Hkv=1, D=256, context 131072, page 1728 (76 relocated pages), "
+               "E4M3 K/V per-tensor scales, fp16 Q/out",
+    "c3_64k": "verify q=8, Hq=6/Hkv=1, D=256, context 65536, page 1728",
+    "c3_256k": "verify q=8, Hq=6/Hkv=1, D=256, context 262144, page 1728",
+    "c2": "verify q=8, Hq=6/Hkv=1, D=256, context 8192, page 3296",
+    "c1": "verify q=2, Hq=6/Hkv=1, D=256, context 1024, page 16",
+    "c4": "64 decode requests q=1, Hq=32/Hkv=8, D=128, log-uniform contexts 512..65536, page 16",
+    "c5": "QSA sparse verify 4 x q=4, Hq=24/Hkv=2, D=128, 512 four-token microblocks per row of 131072",
+}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampler running around the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period), "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for (t, s) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = sorted(float(s[1]) for s in win if s[1].replace(".", "").isdigit())
+        smax = [float(s[2]) for s in win if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in win:
+            for k, n in enumerate(names):
+                if s[5 + k].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch.distributed as dist
+
+    from fp8_e4m3_paged_gb300 import build_lib
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or ws == 1:
+        build_lib.build()
+    if ws > 1:
+        dist.barrier()
+        build_lib.build()
+    from fp8_e4m3_paged_gb300.device_problem import DeviceProblem
+
+    p = make_problem(args.workload)
+    bytes_step = attended_kv_bytes(p)
+    kv_bytes = p.k_cache.numel() + p.v_cache.numel()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    copies = max(2, math.ceil(3 * l2 / max(kv_bytes, 1)) + 1) if args.copies == 0 else args.copies
+    dp = DeviceProblem(p, kv_copies=copies)
+    torch.cuda.synchronize()
+
+    s = torch.cuda.Stream()
+    graphs, split_graphs = [], []
+    with torch.cuda.stream(s):
+        for c in range(copies):
+            dp.run(c)  # first launches (kernel attributes) outside capture
+    torch.cuda.synchronize()
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            dp.run(c)
+        graphs.append(g)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=s):
+            dp.calls[c].split(torch.cuda.current_stream().cuda_stream)
+        split_graphs.append(g2)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(s):
+        for i in range(args.warmup):
+            graphs[i % copies].replay()
+    torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- timed
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for i in range(args.steps):
+            graphs[i % copies].replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # split kernel alone (same stream, same rotation) for the roofline line
+    k2 = max(args.steps // 2, 10)
+    with torch.cuda.stream(s):
+        for i in range(min(args.warmup, 50)):
+            split_graphs[i % copies].replay()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for i in range(k2):
+            split_graphs[i % copies].replay()
+        f1.record(s)
+    torch.cuda.synchronize()
+    split_ms = f0.elapsed_time(f1) / k2
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    # ---------------------------------------------------------------- e2e
+    e2e = run_e2e(p, dp, args, s, bytes_step)
+
+    status = dp.status()
+    peak, peak_src = _peaks()
+    value_gbs = bytes_step * ws / (ms * 1e-3) / 1e9
+    alg_split = bytes_step + p.q_fp16.numel() * 2 + (p.block_table.numel() * 4 + p.row_len.numel() * 4
+                                                      if p.mode == "dense" else
+                                                      p.entry_tbl.numel() * 8 + p.n_entries.numel() * 4)
+    achieved = alg_split / (split_ms * 1e-3) / 1e9
+    traffic = _traffic_record(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value_gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 6),
+        "us_per_step": round(ms * 1e3, 3),
+        "pct_of_hbm_peak": round(100.0 * value_gbs / ws / peak, 2),
+        "hbm_peak_gbs": peak,
+        "hbm_peak_source": peak_src,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; E4M3 bytes from N(0,1) with per-tensor scales)",
+        "config": {
+            "workload": f"{args.workload}: {WORKLOAD_DESC.get(args.workload, '')}",
+            "attended_kv_bytes_per_step": bytes_step,
+            "kernel": ["generic", "tcgen05"][dp.plan.kernel] if dp.plan.kernel < 2 else str(dp.plan.kernel),
+            "num_splits": dp.plan.num_splits,
+            "l2": f"inputs larger than L2: {copies} rotating KV copies, {copies * kv_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "split",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_split,
+            "avg_launch_us": round(split_ms * 1e3, 3),
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+        },
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "device_status": status,
+        "context_pages_v100_fp32_route_ms_at_131072": 0.7916,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p, bytes_step, budget_s=args.cpu_budget)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _traffic_record(workload):
+    """DRAM bytes per split launch from the committed ncu summary, if it
+    matches the current kernel revision (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(workload)
+        if rec and rec.get("kernel_rev") == _kernel_rev():
+            return rec.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def _kernel_rev():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_e4m3_paged_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def run_e2e(p, dp, args, s, bytes_step):
+    """Same metric through the public API with host inputs: every step copies
+    the step's inputs from pinned host memory (Q, the KV pool, the block table
+    and row lengths), runs split + combine, and reads the fp16 output back."""
+    host = {
+        "q": p.q_fp16.pin_memory(),
+        "k": p.k_cache.pin_memory(),
+        "v": p.v_cache.pin_memory(),
+    }
+    if p.mode == "dense":
+        host["bt"] = p.block_table.pin_memory()
+        host["rl"] = p.row_len.pin_memory()
+    else:
+        host["et"] = p.entry_tbl.pin_memory()
+        host["em"] = p.entry_mask.pin_memory()
+        host["ne"] = p.n_entries.pin_memory()
+    out_h = torch.empty(dp.out.shape, dtype=dp.out.dtype).pin_memory()
+    dev = {"q": dp.q, "k": dp.k_caches[0], "v": dp.v_caches[0]}
+    if p.mode == "dense":
+        dev["bt"], dev["rl"] = dp.block_table, dp.row_len
+    else:
+        dev["et"], dev["em"], dev["ne"] = dp.entry_tbl, dp.entry_mask, dp.n_entries
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    steps = max(3, min(args.e2e_steps, args.steps))
+
+    def step():
+        for k, t in host.items():
+            dev[k].copy_(t, non_blocking=True)
+        dp.calls[0].run(torch.cuda.current_stream().cuda_stream)
+        out_h.copy_(dp.out, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            step()
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(p, bytes_step, budget_s=15.0):
+    """The FP64 oracle on the host cores over whole steps of the workload."""
+    import oracle
+
+    threads = oracle.default_threads()
+    oracle.build()
+    t0 = time.time()
+    reps = 0
+    while True:
+        oracle.attention(p, threads=threads)
+        reps += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": round(bytes_step * reps / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{reps} full step(s) of the workload (all query rows and heads)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample (a
+    subset of the workload's query vectors), sized so the whole run stays
+    within a few minutes."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    threads = oracle.default_threads()
+    p = make_problem(args.workload)
+    bytes_step = attended_kv_bytes(p)
+    allitems = [(b, r, h) for b in range(p.B) for r in range(p.q) for h in range(p.Hq)]
+    # cost of one query vector
+    t = time.time()
+    oracle.attention_items(p, [allitems[0]], threads=1)
+    per_item = max(time.time() - t, 1e-4)
+    budget = args.ref_budget / max(1, args.steps + args.warmup)
+    n = int(max(1, min(len(allitems), budget * threads / per_item)))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.attention_items(p, [allitems[i] for i in rng.choice(len(allitems), n, replace=False)], threads=threads)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.attention_items(p, [allitems[i] for i in rng.choice(len(allitems), n, replace=False)], threads=threads)
+    dt = time.time() - t0
+    ms = dt * 1e3 / args.steps
+    frac = n / len(allitems)
+    value = bytes_step * frac / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; E4M3 bytes from N(0,1) with per-tensor scales)",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_DESC.get(args.workload, '')}",
+                   "attended_kv_bytes_per_step": bytes_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {len(allitems)} query vectors per step (random subset), "
+                                   f"scaled to the workload by that fraction"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3_128k")
+    ap.add_argument("--copies", type=int, default=0, help="KV copies to rotate (0 = enough to defeat L2)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

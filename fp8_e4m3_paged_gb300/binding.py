@@ -1,0 +1,193 @@
+"""ctypes binding of libfp8kv_attn.so (the C ABI in include/fp8kv_attn.h).
+
+Argument marshalling only: every step of the attention runs in the library's
+CUDA kernels.  Importing this module loads the in-tree shared library and
+raises ImportError if it has not been built -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8kv_attn.so")
+
+REVISION = 1
+OK = 0
+EINVAL = -1
+EUNSUPPORTED = -2
+EWORKSPACE = -3
+EVERSION = -4
+ECUDA = -5
+
+MODE_DENSE = 0
+MODE_SPARSE_PAGE4 = 1
+
+STATUS_BAD_BLOCK = 0x1
+STATUS_BAD_LEN = 0x2
+STATUS_BAD_ENTRIES = 0x4
+STATUS_TIMEOUT = 0x8
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "mode", "batch", "q_max", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
+        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits")]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "revision", "mode", "batch", "q_max", "num_q_heads", "num_kv_heads", "head_dim",
+        "page_size", "max_kv_len", "max_blocks", "num_kv_blocks", "group", "rows",
+        "num_splits", "tile_tokens", "kernel")] + [
+        ("grid", ctypes.c_int32 * 3),
+        ("block_threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+        ("row_chunk", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+        ("partial_offset", ctypes.c_int64), ("ml_offset", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64),
+        ("reserved", ctypes.c_int32 * 16),
+    ]
+
+
+class Args(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("k_stride_block", ctypes.c_int64), ("k_stride_token", ctypes.c_int64),
+        ("k_stride_head", ctypes.c_int64),
+        ("v_stride_block", ctypes.c_int64), ("v_stride_token", ctypes.c_int64),
+        ("v_stride_head", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int64),
+        ("row_kv_len", ctypes.c_void_p),
+        ("entry_tbl", ctypes.c_void_p), ("entry_mask", ctypes.c_void_p),
+        ("n_entries", ctypes.c_void_p), ("entry_stride", ctypes.c_int64),
+        ("softmax_scale", ctypes.c_float), ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
+        ("k_scale_dev", ctypes.c_void_p), ("v_scale_dev", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m fp8_e4m3_paged_gb300.build_lib` "
+        "(the CUDA library is required; there is no CPU fallback)")
+
+lib = ctypes.CDLL(LIB_PATH)
+lib.fp8kv_attn_version.restype = ctypes.c_int
+lib.fp8kv_attn_version.argtypes = []
+lib.fp8kv_attn_strerror.restype = ctypes.c_char_p
+lib.fp8kv_attn_strerror.argtypes = [ctypes.c_int]
+lib.fp8kv_attn_plan.restype = ctypes.c_int
+lib.fp8kv_attn_plan.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Plan)]
+for _n in ("fp8kv_attn_split", "fp8kv_attn_combine"):
+    getattr(lib, _n).restype = ctypes.c_int
+    getattr(lib, _n).argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), ctypes.c_void_p]
+
+
+class Fp8kvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {fp8kv_attn_strerror(code)} ({code})")
+
+
+def fp8kv_attn_version() -> int:
+    return lib.fp8kv_attn_version()
+
+
+def fp8kv_attn_strerror(code: int) -> str:
+    return lib.fp8kv_attn_strerror(code).decode()
+
+
+def fp8kv_attn_plan(desc: Desc) -> Plan:
+    plan = Plan()
+    rc = lib.fp8kv_attn_plan(ctypes.byref(desc), ctypes.byref(plan))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_plan")
+    return plan
+
+
+def fp8kv_attn_split(plan: Plan, args: Args, stream: int = 0) -> None:
+    rc = lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(args), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_split")
+
+
+def fp8kv_attn_combine(plan: Plan, args: Args, stream: int = 0) -> None:
+    rc = lib.fp8kv_attn_combine(ctypes.byref(plan), ctypes.byref(args), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_combine")
+
+
+# ---------------------------------------------------------------- torch glue
+
+def make_desc(*, mode: int, batch: int, q_max: int, num_q_heads: int, num_kv_heads: int,
+              head_dim: int, page_size: int, max_kv_len: int, max_blocks: int,
+              num_kv_blocks: int, num_sms: int = 0, num_splits: int = 0) -> Desc:
+    return Desc(mode, batch, q_max, num_q_heads, num_kv_heads, head_dim, page_size,
+                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def make_args(*, q, k_cache, v_cache, out, workspace, softmax_scale: float,
+              k_scale: float = 1.0, v_scale: float = 1.0,
+              block_table=None, row_kv_len=None,
+              entry_tbl=None, entry_mask=None, n_entries=None,
+              k_scale_dev=None, v_scale_dev=None) -> Args:
+    """Fill an Args struct from torch CUDA tensors.
+
+    k_cache / v_cache: uint8 tensors indexed [block][slot][kv_head][d] (any
+    strides with d contiguous); q / out: fp16 [B][q_max][Hq][D] contiguous;
+    workspace: a uint8 tensor of at least plan.workspace_bytes bytes.
+    """
+    a = Args()
+    a.q = _ptr(q)
+    a.k_cache = _ptr(k_cache)
+    a.v_cache = _ptr(v_cache)
+    ks = k_cache.stride()
+    vs = v_cache.stride()
+    eb_k = k_cache.element_size()
+    eb_v = v_cache.element_size()
+    a.k_stride_block, a.k_stride_token, a.k_stride_head = ks[0] * eb_k, ks[1] * eb_k, ks[2] * eb_k
+    a.v_stride_block, a.v_stride_token, a.v_stride_head = vs[0] * eb_v, vs[1] * eb_v, vs[2] * eb_v
+    if block_table is not None:
+        a.block_table = _ptr(block_table)
+        a.block_table_stride = block_table.stride(0)
+    a.row_kv_len = _ptr(row_kv_len)
+    if entry_tbl is not None:
+        a.entry_tbl = _ptr(entry_tbl)
+        a.entry_stride = entry_tbl.stride(0)
+    a.entry_mask = _ptr(entry_mask)
+    a.n_entries = _ptr(n_entries)
+    a.softmax_scale = float(softmax_scale)
+    a.k_scale = float(k_scale)
+    a.v_scale = float(v_scale)
+    a.k_scale_dev = _ptr(k_scale_dev)
+    a.v_scale_dev = _ptr(v_scale_dev)
+    a.out = _ptr(out)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return a
+
+
+@dataclass
+class Call:
+    """A planned split + combine over fixed device buffers (graph friendly)."""
+    plan: Plan
+    args: Args
+
+    def split(self, stream: int) -> None:
+        fp8kv_attn_split(self.plan, self.args, stream)
+
+    def combine(self, stream: int) -> None:
+        fp8kv_attn_combine(self.plan, self.args, stream)
+
+    def run(self, stream: int) -> None:
+        self.split(stream)
+        self.combine(stream)

@@ -1,0 +1,213 @@
+// C ABI entry points: planning (host only), argument validation, dispatch.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "fp8kv_attn.h"
+#include "internal.h"
+
+using namespace fp8kv;
+
+namespace {
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+
+extern "C" int fp8kv_attn_version(void) { return FP8KV_ATTN_REVISION; }
+
+extern "C" const char* fp8kv_attn_strerror(int code) {
+  switch (code) {
+    case FP8KV_OK: return "ok";
+    case FP8KV_EINVAL: return "invalid argument (null or misaligned pointer, bad shape or stride)";
+    case FP8KV_EUNSUPPORTED: return "unsupported shape (head_dim, q_max, or sparse page size)";
+    case FP8KV_EWORKSPACE: return "workspace smaller than the plan requires";
+    case FP8KV_EVERSION: return "plan was built by another library revision";
+    case FP8KV_ECUDA: return "CUDA runtime error";
+    default: return "unknown error code";
+  }
+}
+
+extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan) {
+  if (!d || !plan) return FP8KV_EINVAL;
+  if (d->mode != FP8KV_MODE_DENSE && d->mode != FP8KV_MODE_SPARSE_PAGE4) return FP8KV_EINVAL;
+  if (d->batch < 0 || d->num_q_heads < 1 || d->num_kv_heads < 1) return FP8KV_EINVAL;
+  if (d->num_q_heads % d->num_kv_heads) return FP8KV_EINVAL;
+  if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return FP8KV_EUNSUPPORTED;
+  if (d->q_max < 1) return FP8KV_EINVAL;
+  if (d->q_max > 16) return FP8KV_EUNSUPPORTED;
+  if (d->page_size < 1 || d->max_kv_len < 0 || d->max_blocks < 0 || d->num_kv_blocks < 1)
+    return FP8KV_EINVAL;
+  if (d->num_sms < 0 || d->num_splits < 0) return FP8KV_EINVAL;
+  if (d->mode == FP8KV_MODE_DENSE) {
+    if ((int64_t)d->max_blocks * d->page_size < d->max_kv_len) return FP8KV_EINVAL;
+  } else {
+    if (d->page_size != 4 || d->q_max > 8) return FP8KV_EUNSUPPORTED;
+  }
+
+  int sms = d->num_sms;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8KV_ECUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FP8KV_ECUDA;
+    if (sms < 1) return FP8KV_ECUDA;
+  }
+
+  fp8kv_attn_plan_t P;
+  std::memset(&P, 0, sizeof(P));
+  P.revision = FP8KV_ATTN_REVISION;
+  P.mode = d->mode;
+  P.batch = d->batch;
+  P.q_max = d->q_max;
+  P.num_q_heads = d->num_q_heads;
+  P.num_kv_heads = d->num_kv_heads;
+  P.head_dim = d->head_dim;
+  P.page_size = d->page_size;
+  P.max_kv_len = d->max_kv_len;
+  P.max_blocks = d->max_blocks;
+  P.num_kv_blocks = d->num_kv_blocks;
+  P.group = d->num_q_heads / d->num_kv_heads;
+  P.rows = d->q_max * P.group;
+  P.num_sms = sms;
+
+  // Generic CUDA-core path.
+  P.kernel = kGeneric;
+  P.row_chunk = P.rows < kMaxRowChunk ? P.rows : kMaxRowChunk;
+  const int n_chunks = ceil_div(P.rows, P.row_chunk);
+  P.tile_tokens = kGenericTileTokens;
+  P.block_threads = kGenericThreads;
+  P.smem_bytes = generic_smem_bytes(P.head_dim, P.row_chunk);
+
+  // Split count: enough CTAs for about two waves, never more partitions than
+  // tiles of work (dense: tokens / 32, sparse: entries / 8).
+  const int64_t units = (int64_t)d->batch * d->num_kv_heads * n_chunks;
+  const int max_tiles = d->mode == FP8KV_MODE_DENSE
+                            ? (d->max_kv_len > 0 ? ceil_div(d->max_kv_len, kGenericTileTokens) : 1)
+                            : (d->max_blocks > 0 ? ceil_div(d->max_blocks, kGenericTileTokens / 4) : 1);
+  int S;
+  if (d->num_splits > 0) {
+    S = d->num_splits;
+  } else {
+    const int64_t target = 2LL * sms;
+    S = units > 0 ? ceil_div(target, units) : 1;
+    if (S > max_tiles) S = max_tiles;
+    if (S < 1) S = 1;
+  }
+  P.num_splits = S;
+  P.grid[0] = S;
+  P.grid[1] = d->num_kv_heads * n_chunks;
+  P.grid[2] = d->batch;
+
+  const int64_t nvec = (int64_t)d->batch * d->num_kv_heads * S * P.rows;
+  P.partial_offset = 256;
+  P.ml_offset = align_up(P.partial_offset + nvec * P.head_dim * 4, 256);
+  P.workspace_bytes = align_up(P.ml_offset + nvec * 8, 256);
+  *plan = P;
+  return FP8KV_OK;
+}
+
+int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params* p) {
+  if (!plan || !a || !p) return FP8KV_EINVAL;
+  if (plan->revision != FP8KV_ATTN_REVISION) return FP8KV_EVERSION;
+  std::memset(p, 0, sizeof(*p));
+  p->mode = plan->mode;
+  p->B = plan->batch;
+  p->q_max = plan->q_max;
+  p->Hq = plan->num_q_heads;
+  p->Hkv = plan->num_kv_heads;
+  p->D = plan->head_dim;
+  p->G = plan->group;
+  p->rows = plan->rows;
+  p->row_chunk = plan->row_chunk;
+  p->n_row_chunks = plan->row_chunk > 0 ? (plan->rows + plan->row_chunk - 1) / plan->row_chunk : 0;
+  p->S = plan->num_splits;
+  p->page_size = plan->page_size;
+  p->max_kv_len = plan->max_kv_len;
+  p->max_blocks = plan->max_blocks;
+  p->num_kv_blocks = plan->num_kv_blocks;
+  if (p->G < 1 || p->rows != p->q_max * p->G || p->S < 1 || p->row_chunk < 1) return FP8KV_EINVAL;
+
+  if (!a->workspace || !aligned(a->workspace, 256)) return FP8KV_EINVAL;
+  if ((int64_t)a->workspace_bytes < plan->workspace_bytes) return FP8KV_EWORKSPACE;
+  if (p->B == 0) {
+    p->status = reinterpret_cast<unsigned int*>(a->workspace);
+    return FP8KV_OK;
+  }
+  if (!a->q || !a->out || !a->k_cache || !a->v_cache) return FP8KV_EINVAL;
+  if (!aligned(a->q, 16) || !aligned(a->out, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16))
+    return FP8KV_EINVAL;
+  const int64_t st[6] = {a->k_stride_block, a->k_stride_token, a->k_stride_head,
+                         a->v_stride_block, a->v_stride_token, a->v_stride_head};
+  for (int64_t s : st)
+    if (s < 0 || (s % 16) != 0) return FP8KV_EINVAL;
+  if (plan->mode == FP8KV_MODE_DENSE) {
+    if (!a->block_table || !a->row_kv_len) return FP8KV_EINVAL;
+    if (a->block_table_stride < plan->max_blocks || a->block_table_stride < 1) return FP8KV_EINVAL;
+  } else {
+    if (!a->entry_tbl || !a->entry_mask || !a->n_entries) return FP8KV_EINVAL;
+    if (a->entry_stride < plan->max_blocks || a->entry_stride < 1) return FP8KV_EINVAL;
+  }
+  if (!std::isfinite(a->softmax_scale)) return FP8KV_EINVAL;
+  if (!a->k_scale_dev && !std::isfinite(a->k_scale)) return FP8KV_EINVAL;
+  if (!a->v_scale_dev && !std::isfinite(a->v_scale)) return FP8KV_EINVAL;
+
+  p->q = reinterpret_cast<const uint16_t*>(a->q);
+  p->k_cache = a->k_cache;
+  p->v_cache = a->v_cache;
+  p->ksb = a->k_stride_block;
+  p->kst = a->k_stride_token;
+  p->ksh = a->k_stride_head;
+  p->vsb = a->v_stride_block;
+  p->vst = a->v_stride_token;
+  p->vsh = a->v_stride_head;
+  p->block_table = a->block_table;
+  p->bt_stride = a->block_table_stride;
+  p->row_len = a->row_kv_len;
+  p->entry_tbl = a->entry_tbl;
+  p->entry_mask = a->entry_mask;
+  p->n_entries = a->n_entries;
+  p->entry_stride = a->entry_stride;
+  p->softmax_scale = a->softmax_scale;
+  p->k_scale = a->k_scale;
+  p->v_scale = a->v_scale;
+  p->k_scale_dev = a->k_scale_dev;
+  p->v_scale_dev = a->v_scale_dev;
+  p->out = reinterpret_cast<uint16_t*>(a->out);
+  char* ws = reinterpret_cast<char*>(a->workspace);
+  p->status = reinterpret_cast<unsigned int*>(ws);
+  p->partial = reinterpret_cast<float*>(ws + plan->partial_offset);
+  p->ml = reinterpret_cast<float2*>(ws + plan->ml_offset);
+  return FP8KV_OK;
+}
+
+extern "C" int fp8kv_attn_split(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
+                                fp8kv_stream_t stream) {
+  Params p;
+  const int rc = build_params(plan, a, &p);
+  if (rc != FP8KV_OK) return rc;
+  if (p.B == 0) return FP8KV_OK;
+  cudaError_t e;
+  switch (plan->kernel) {
+    case kGeneric: e = launch_split_generic(plan, p, reinterpret_cast<cudaStream_t>(stream)); break;
+    case kTc: e = launch_split_tc(plan, p, reinterpret_cast<cudaStream_t>(stream)); break;
+    default: return FP8KV_EINVAL;
+  }
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}
+
+extern "C" int fp8kv_attn_combine(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
+                                  fp8kv_stream_t stream) {
+  Params p;
+  const int rc = build_params(plan, a, &p);
+  if (rc != FP8KV_OK) return rc;
+  if (p.B == 0) return FP8KV_OK;
+  const cudaError_t e = launch_combine(plan, p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}

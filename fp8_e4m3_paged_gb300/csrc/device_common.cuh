@@ -1,0 +1,56 @@
+// Device helpers shared by the split and combine kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_fp16.h>
+
+namespace fp8kv {
+
+// log2(e): logits are kept in base-2 units so that softmax uses exp2.
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Exact E4M3 -> FP32 for the four bytes of w (little-endian order).
+//
+// An E4M3 byte s.eeee.mmm placed so that eeee lands in the low four bits of
+// the FP32 exponent field and mmm in the top of the FP32 mantissa encodes
+// dec(b) * 2^-120 exactly (normal codes: 2^(e-127) * 1.mmm; subnormal codes
+// e = 0: m * 2^-129 as an FP32 denormal); multiplying by 2^120 is exact.
+// The two NaN codes map to the finite value 480: every byte the kernels read
+// but must not use is excluded by selection, never by arithmetic.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&o)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t b = (w >> (8 * k)) & 0xFFu;
+    const uint32_t bits = ((b & 0x80u) << 24) | ((b & 0x7Fu) << 20);
+    o[k] = __uint_as_float(bits) * 0x1p120f;
+  }
+}
+
+// Exact E4M3 -> fp16 pair for two bytes: result halves hold dec(b) * 2^-8.
+// With the byte in bits 8..15 of a 16-bit lane (h = b << 8), the fp16 pattern
+// is sign(h) | ((h >> 1) & 0x3F80): exponent bits eeee become the low four
+// bits of the fp16 exponent (bias 15 vs 7: a factor 2^-8) and mmm the top of
+// the fp16 mantissa; subnormals map to fp16 subnormals exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_lo(uint32_t w) {
+  // bytes 0,1 of w -> halves 0,1
+  const uint32_t h = __byte_perm(w, 0u, 0x1404u);  // [b1,0,b0,0] as bytes 3..0
+  return (h & 0x80008000u) | ((h >> 1) & 0x3F803F80u);
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_hi(uint32_t w) {
+  // bytes 2,3 of w -> halves 0,1
+  const uint32_t h = __byte_perm(w, 0u, 0x3424u);
+  return (h & 0x80008000u) | ((h >> 1) & 0x3F803F80u);
+}
+
+__device__ __forceinline__ void set_status(unsigned int* status, unsigned int bit) {
+  atomicOr(status, bit);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace fp8kv

@@ -1,0 +1,76 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <atomic>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "fp8kv_attn.h"
+
+namespace fp8kv {
+
+// Split-kernel variants a plan may choose.
+enum Kernel : int32_t {
+  kGeneric = 0,  // CUDA-core FP32 path, any supported shape
+  kTc = 1,       // tcgen05 tensor-core path (dense and sparse, rows <= 64)
+};
+
+constexpr int kGenericThreads = 256;
+constexpr int kGenericTileTokens = 32;  // tokens (dense) or 8 entries (sparse)
+constexpr int kMaxRowChunk = 64;        // query vectors per split CTA
+
+// Everything a split or combine kernel needs, resolved on the host.
+struct Params {
+  // problem
+  int32_t mode, B, q_max, Hq, Hkv, D, G, rows, row_chunk, n_row_chunks, S;
+  int32_t page_size, max_kv_len, max_blocks, num_kv_blocks;
+  // inputs
+  const uint16_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  int64_t ksb, kst, ksh, vsb, vst, vsh;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* row_len;
+  const int32_t* entry_tbl;
+  const uint32_t* entry_mask;
+  const int32_t* n_entries;
+  int64_t entry_stride;
+  // scales: logit factor = softmax_scale * k_scale * log2(e)
+  float softmax_scale, k_scale, v_scale;
+  const float* k_scale_dev;
+  const float* v_scale_dev;
+  // outputs / workspace
+  uint16_t* out;
+  unsigned int* status;
+  float* partial;   // [B][Hkv][S][rows][D]
+  float2* ml;       // [B][Hkv][S][rows]  (max in log2 units, sum)
+};
+
+int build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params* p);
+
+cudaError_t launch_split_generic(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
+cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
+cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
+
+// Runs a setup call (a kernel attribute) once per device, on first use.
+struct DeviceOnce {
+  std::atomic<uint64_t> done{0};
+  template <class F>
+  cudaError_t run(F f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = f();
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+};
+
+// Shared-memory bytes of the generic split kernel for a head dim and row chunk.
+int generic_smem_bytes(int D, int row_chunk);
+
+}  // namespace fp8kv

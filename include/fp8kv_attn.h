@@ -1,0 +1,186 @@
+/*
+ * fp8kv_attn.h -- C ABI of a paged-attention library for an FP8 E4M3 KV cache
+ * (one GPU, sm_103a).
+ *
+ * What the calls compute
+ * ----------------------
+ * For every request b, query row r < q_max and query head h, with KV head
+ * g = h / (Hq / Hkv), softmax attention over the tokens the row may see:
+ *
+ *   z_j   = softmax_scale * k_scale * <q[b][r][h], dec(K_j)>
+ *   out   = v_scale * sum_j softmax(z)_j * dec(V_j)          (fp16, RNE)
+ *
+ * where dec() is the exact E4M3 (OCP E4M3FN) decode of the cache bytes.
+ *  - Dense mode: row r sees tokens [0, row_kv_len[b][r]); token t lives in
+ *    physical block block_table[b][t / page_size], slot t % page_size.  A row
+ *    length of 0 is a dead row and yields +0.0.  (Live per-query lengths
+ *    including zero padding, runtime page stride: "DFlash2 E4M3 attention
+ *    with FP32 state", intro paragraphs 3 and 5.)
+ *  - Sparse mode (QSA): four-token microblocks.  Entry e < n_entries[b] names
+ *    physical microblock entry_tbl[b][e]; bit (4*r + t) of entry_mask[b][e]
+ *    says that query row r sees token t of it.  Entries with mask 0 (the null
+ *    padding entries) are never read, and unseen tokens contribute exactly
+ *    zero whatever their bytes decode to, NaN included.  ("Qualify calibrated
+ *    E4M3 and disk PLE with QSA DCP2", commit "grouped page4 null-block
+ *    padding"; "Qwen4Exp: fp8_e4m3 main KV cache on the QSA path".)
+ *  - Scales: the K scale is folded into the logit scale and the V scale is
+ *    an output scale, both applied outside the token loop ("Qwen4Exp: fp8_e4m3
+ *    main KV cache on the QSA path", review thread on host-side KV scales).
+ *
+ * Numerical contract ("DFlash2 E4M3 attention with FP32 state", intro
+ * paragraph 4): FP32 QK and PV accumulation; split-KV partitions store FP32
+ * unnormalised numerators with a separate FP32 running max and sum; an FP32
+ * combine writes the FP16 output.
+ *
+ * Calls
+ * -----
+ *   fp8kv_attn_plan     host only: validates a shape and picks the split
+ *                       count, grid and workspace size.
+ *   fp8kv_attn_split    launches the split kernel (partials into workspace).
+ *   fp8kv_attn_combine  launches the combine kernel (workspace -> out).
+ *
+ * split and combine must run on the same stream with the same workspace; one
+ * workspace serves one stream at a time.  The library never allocates, frees,
+ * synchronises, or reads device memory from the host, and keeps no state
+ * between calls apart from a once-per-device kernel attribute setting, so a
+ * split + combine pair can be captured in a CUDA graph and replayed with new
+ * row lengths, masks or entry counts in the same device buffers.
+ *
+ * Errors: every call returns FP8KV_OK (0) or a negative FP8KV_E* code and
+ * never aborts.  Device-side anomalies never trap: an out-of-range block id or
+ * microblock id contributes nothing, a length or entry count above the planned
+ * bound is clamped, and a sticky FP8KV_STATUS_* bit is OR-ed into the 32-bit
+ * status word at byte offset 0 of the workspace.  The caller zeroes that word
+ * (e.g. once, with the rest of the workspace) and may read it after a sync.
+ */
+#ifndef FP8KV_ATTN_H
+#define FP8KV_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Capability revision: a plan records the revision that built it and the
+ * launch calls refuse a plan from another revision (FP8KV_EVERSION), so a
+ * stale plan cannot reach kernels with another partial layout ("DFlash2 E4M3
+ * attention with FP32 state", intro paragraph 5: the wrapper requires a given
+ * precision capability revision). */
+#define FP8KV_ATTN_REVISION 1
+
+/* Return codes. */
+#define FP8KV_OK 0
+#define FP8KV_EINVAL (-1)       /* null or misaligned pointer, bad shape or stride */
+#define FP8KV_EUNSUPPORTED (-2) /* head_dim, q_max, or sparse with page_size != 4 */
+#define FP8KV_EWORKSPACE (-3)   /* workspace smaller than plan->workspace_bytes */
+#define FP8KV_EVERSION (-4)     /* plan built by another revision */
+#define FP8KV_ECUDA (-5)        /* a CUDA runtime call or launch failed */
+
+/* Modes. */
+#define FP8KV_MODE_DENSE 0
+#define FP8KV_MODE_SPARSE_PAGE4 1
+
+/* Sticky device status bits (workspace word at byte offset 0). */
+#define FP8KV_STATUS_BAD_BLOCK 0x1   /* block / microblock id outside [0, num_kv_blocks) */
+#define FP8KV_STATUS_BAD_LEN 0x2     /* a row length < 0 or > max_kv_len (clamped) */
+#define FP8KV_STATUS_BAD_ENTRIES 0x4 /* n_entries < 0 or > max_blocks (clamped) */
+#define FP8KV_STATUS_TIMEOUT 0x8     /* a bounded pipeline wait gave up */
+
+/* cudaStream_t without including CUDA headers (same type). */
+typedef struct CUstream_st* fp8kv_stream_t;
+
+/* Problem shape (host memory, read only during fp8kv_attn_plan). */
+typedef struct {
+  int32_t mode;          /* FP8KV_MODE_* */
+  int32_t batch;         /* B >= 0 requests (0: nothing to do) */
+  int32_t q_max;         /* query rows per request: 1..16 dense, 1..8 sparse */
+  int32_t num_q_heads;   /* Hq >= 1 */
+  int32_t num_kv_heads;  /* Hkv >= 1, Hq % Hkv == 0 */
+  int32_t head_dim;      /* D: 64, 128 or 256 */
+  int32_t page_size;     /* tokens per physical block, >= 1 (sparse: 4) */
+  int32_t max_kv_len;    /* dense: upper bound of every row_kv_len; sparse: unused */
+  int32_t max_blocks;    /* dense: block-table columns used per request (>= ceil(max_kv_len/page_size));
+                            sparse: entry slots per request (upper bound of n_entries) */
+  int32_t num_kv_blocks; /* physical blocks in the page pool (for bounds checks), >= 1 */
+  int32_t num_sms;       /* SMs to plan for; 0 = ask the current device */
+  int32_t num_splits;    /* split-KV partitions per (request, KV head); 0 = planner's choice */
+} fp8kv_attn_desc;
+
+/* A plan: plain data, owned by the caller, nothing to free.  Fields other than
+ * `reserved` are informational; pass the plan back unmodified. */
+typedef struct {
+  int32_t revision;      /* FP8KV_ATTN_REVISION of the library that planned it */
+  int32_t mode, batch, q_max, num_q_heads, num_kv_heads, head_dim, page_size;
+  int32_t max_kv_len, max_blocks, num_kv_blocks;
+  int32_t group;         /* Hq / Hkv */
+  int32_t rows;          /* q_max * group: query vectors per (request, KV head) */
+  int32_t num_splits;    /* S */
+  int32_t tile_tokens;   /* tokens per pipeline tile (dense) */
+  int32_t kernel;        /* split-kernel variant chosen */
+  int32_t grid[3];       /* split-kernel grid */
+  int32_t block_threads; /* split-kernel block size */
+  int32_t smem_bytes;    /* split-kernel dynamic shared memory */
+  int32_t row_chunk;     /* query vectors per split CTA */
+  int32_t num_sms;
+  int64_t partial_offset;  /* byte offset of FP32 numerators in the workspace */
+  int64_t ml_offset;       /* byte offset of FP32 (max, sum) pairs */
+  int64_t workspace_bytes; /* minimum workspace size */
+  int32_t reserved[16];
+} fp8kv_attn_plan_t;
+
+/* Per-call arguments.  All pointers are device pointers owned by the caller,
+ * except that the struct itself lives in host memory. */
+typedef struct {
+  const void* q;            /* fp16 [B][q_max][Hq][D], contiguous, 16-byte aligned */
+  const uint8_t* k_cache;   /* E4M3 bytes; element (block, slot, kv head, d) at
+                               k_cache + block*k_stride_block + slot*k_stride_token
+                               + head*k_stride_head + d  (d contiguous) */
+  const uint8_t* v_cache;   /* same addressing with the v_stride_* values */
+  int64_t k_stride_block, k_stride_token, k_stride_head; /* bytes, multiples of 16 */
+  int64_t v_stride_block, v_stride_token, v_stride_head; /* bytes, multiples of 16 */
+  const int32_t* block_table;   /* dense: [B][block_table_stride] physical block ids */
+  int64_t block_table_stride;   /* elements */
+  const int32_t* row_kv_len;    /* dense: [B][q_max] live lengths (0 = dead row) */
+  const int32_t* entry_tbl;     /* sparse: [B][entry_stride] microblock ids */
+  const uint32_t* entry_mask;   /* sparse: [B][entry_stride] visibility bits (4*r + t) */
+  const int32_t* n_entries;     /* sparse: [B] entries in use */
+  int64_t entry_stride;         /* elements */
+  float softmax_scale;          /* logit scale before the K scale */
+  float k_scale;                /* host K scale (used when k_scale_dev is NULL) */
+  float v_scale;                /* host V scale (used when v_scale_dev is NULL) */
+  const float* k_scale_dev;     /* optional device scalar (one float), NULL = host */
+  const float* v_scale_dev;     /* optional device scalar (one float), NULL = host */
+  void* out;                    /* fp16 [B][q_max][Hq][D], contiguous */
+  void* workspace;              /* >= plan->workspace_bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} fp8kv_attn_args;
+
+/* Library revision (FP8KV_ATTN_REVISION). */
+int fp8kv_attn_version(void);
+
+/* Static text for a return code; never NULL. */
+const char* fp8kv_attn_strerror(int code);
+
+/* Validate `d` and fill `plan`.  Host only; touches no device memory.  When
+ * d->num_sms is 0 it reads the current device's SM count (FP8KV_ECUDA if that
+ * fails).  Returns FP8KV_EINVAL / FP8KV_EUNSUPPORTED for shapes it rejects. */
+int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan);
+
+/* Launch the split kernel on `stream`: every (request, KV head, partition)
+ * writes FP32 numerators and an FP32 (max, sum) pair per query vector into
+ * the workspace.  Empty partitions write (max = -inf, sum = 0). */
+int fp8kv_attn_split(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
+                     fp8kv_stream_t stream);
+
+/* Launch the combine kernel on `stream`: merges the partitions of every query
+ * vector in FP32 and writes fp16 `out` (rows whose total sum is 0 get +0.0). */
+int fp8kv_attn_combine(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
+                       fp8kv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_ATTN_H */

@@ -1,0 +1,147 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library is built in-tree with nvcc (cross-compiling for sm_103a), loaded,
+and checked to export every function include/fp8kv_attn.h declares.  Planning
+is pure host code and is exercised directly; split/combine are called only
+with arguments the host-side validation rejects, so no kernel is launched.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8kv_attn.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from fp8_e4m3_paged_gb300 import build_lib
+
+    build_lib.build()
+    from fp8_e4m3_paged_gb300 import binding
+
+    return binding
+
+
+def _declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8kv_attn_\w+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(B):
+    names = _declared_functions()
+    assert {"fp8kv_attn_plan", "fp8kv_attn_split", "fp8kv_attn_combine"} <= set(names)
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror(B):
+    assert B.fp8kv_attn_version() == B.REVISION
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(B.fp8kv_attn_strerror(code), str) and B.fp8kv_attn_strerror(code)
+
+
+def _desc(B, **kw):
+    base = dict(mode=B.MODE_DENSE, batch=1, q_max=8, num_q_heads=6, num_kv_heads=1, head_dim=256,
+                page_size=1728, max_kv_len=131072, max_blocks=76, num_kv_blocks=77, num_sms=152)
+    base.update(kw)
+    return B.make_desc(**base)
+
+
+def test_plan_shape_and_workspace(B):
+    p = B.fp8kv_attn_plan(_desc(B))
+    assert p.revision == B.REVISION
+    assert p.group == 6 and p.rows == 48
+    S = p.num_splits
+    assert 1 <= S
+    nvec = 1 * 1 * S * 48
+    assert p.partial_offset >= 4
+    assert p.ml_offset >= p.partial_offset + nvec * 256 * 4
+    assert p.workspace_bytes >= p.ml_offset + nvec * 8
+    assert p.workspace_bytes % 256 == 0
+    assert p.grid[0] * p.grid[1] * p.grid[2] >= 1
+
+
+def test_plan_split_override_and_batch0(B):
+    p = B.fp8kv_attn_plan(_desc(B, num_splits=7))
+    assert p.num_splits == 7
+    p0 = B.fp8kv_attn_plan(_desc(B, batch=0))
+    assert p0.workspace_bytes >= 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), -2),
+    (dict(q_max=17), -2),
+    (dict(q_max=0), -1),
+    (dict(num_q_heads=5, num_kv_heads=2), -1),
+    (dict(page_size=0), -1),
+    (dict(max_blocks=10), -1),
+    (dict(num_kv_blocks=0), -1),
+    (dict(mode=7), -1),
+    (dict(mode=1, page_size=16), -2),
+    (dict(mode=1, page_size=4, q_max=9), -2),
+    (dict(batch=-1), -1),
+    (dict(num_splits=-3), -1),
+])
+def test_plan_rejects(B, kw, code):
+    with pytest.raises(B.Fp8kvError) as ei:
+        B.fp8kv_attn_plan(_desc(B, **kw))
+    assert ei.value.code == code
+
+
+def _fake_args(B, plan, **kw):
+    a = B.Args()
+    fake = 1 << 20  # 16-byte aligned non-null values; never dereferenced on the host
+    a.q = a.k_cache = a.v_cache = a.out = fake
+    a.k_stride_block = a.v_stride_block = 1728 * 256
+    a.k_stride_token = a.v_stride_token = 256
+    a.k_stride_head = a.v_stride_head = 256
+    a.block_table = a.row_kv_len = fake
+    a.block_table_stride = plan.max_blocks
+    a.softmax_scale, a.k_scale, a.v_scale = 0.0625, 1.0, 1.0
+    a.workspace = 1 << 24
+    a.workspace_bytes = plan.workspace_bytes
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1),
+    (dict(k_cache=(1 << 20) + 8), -1),
+    (dict(k_stride_token=250), -1),
+    (dict(block_table=None), -1),
+    (dict(workspace=(1 << 24) + 16), -1),
+    (dict(softmax_scale=float("nan")), -1),
+    (dict(k_scale=float("inf")), -1),
+])
+def test_launch_validation(B, kw, code):
+    plan = B.fp8kv_attn_plan(_desc(B))
+    a = _fake_args(B, plan, **kw)
+    for fn in (B.lib.fp8kv_attn_split, B.lib.fp8kv_attn_combine):
+        assert fn(ctypes.byref(plan), ctypes.byref(a), None) == code
+
+
+def test_launch_workspace_and_revision(B):
+    plan = B.fp8kv_attn_plan(_desc(B))
+    a = _fake_args(B, plan, workspace_bytes=plan.workspace_bytes - 1)
+    assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == B.EWORKSPACE
+    a = _fake_args(B, plan)
+    stale = B.Plan.from_buffer_copy(plan)
+    stale.revision = B.REVISION + 1
+    assert B.lib.fp8kv_attn_split(ctypes.byref(stale), ctypes.byref(a), None) == B.EVERSION
+    assert B.lib.fp8kv_attn_combine(ctypes.byref(stale), ctypes.byref(a), None) == B.EVERSION
+
+
+def test_batch0_launch_is_noop(B):
+    plan = B.fp8kv_attn_plan(_desc(B, batch=0))
+    a = B.Args()
+    a.workspace = 1 << 24
+    a.workspace_bytes = plan.workspace_bytes
+    assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == 0
+    assert B.lib.fp8kv_attn_combine(ctypes.byref(plan), ctypes.byref(a), None) == 0

@@ -1,0 +1,221 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Every named workload runs through fp8kv_attn_plan / _split / _combine on
+cuda:0 and is compared element by element with the oracle on the same seeded
+bytes (tests/_check.py: rel L2 <= 5e-4, <= 4 fp16 ulps, no NaN/Inf).  The
+batched decode workload (1.76 GB of cache) is compared on sampled query
+vectors; everything else in full.  Edge cases: forced split counts, graph
+replay with live lengths 8 -> 5 -> 0, bitwise determinism across replays,
+NaN and 448 poisoning of padding / unused slots, dead rows, device-side
+scales, interleaved K/V strides, out-of-range block ids and lengths.
+"""
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import make_dense, make_problem, make_sparse
+from synth.workloads import POISON_MAX, POISON_NAN, causal_row_len
+from tests._check import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fp8_e4m3_paged_gb300 import build_lib
+
+    build_lib.build()
+    oracle.build()
+
+
+def _dp(p, **kw):
+    from fp8_e4m3_paged_gb300.device_problem import DeviceProblem
+
+    return DeviceProblem(p, **kw)
+
+
+@functools.lru_cache(maxsize=None)
+def _problem(name, poison=POISON_NAN):
+    return make_problem(name, poison=poison)
+
+
+@functools.lru_cache(maxsize=None)
+def _ref(name, poison=POISON_NAN):
+    return oracle.attention(_problem(name, poison))
+
+
+def _run(dp):
+    out = dp.run()
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3_64k", "c3_128k", "c3_256k", "c5"])
+def test_named_workload(name):
+    p = _problem(name)
+    dp = _dp(p)
+    got = _run(dp)
+    compare(got, _ref(name), what=name)
+    assert dp.status() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 40, 500])
+def test_c2_forced_splits(splits):
+    p = _problem("c2")
+    got = _run(_dp(p, num_splits=splits))
+    compare(got, _ref("c2"), what=f"c2 S={splits}")
+
+
+@pytest.mark.parametrize("name,poison", [("c2", POISON_MAX), ("c1", POISON_MAX), ("c5", POISON_MAX)])
+def test_poisoned_padding(name, poison):
+    p = _problem(name, poison)
+    got = _run(_dp(p))
+    compare(got, _ref(name, poison), what=f"{name} poison {poison:#x}")
+
+
+def test_c4_sampled():
+    p = _problem("c4")
+    dp = _dp(p)
+    got = _run(dp)
+    assert np.isfinite(got).all()
+    g = torch.Generator().manual_seed(7)
+    n = 384
+    b = torch.randint(0, p.B, (n,), generator=g)
+    h = torch.randint(0, p.Hq, (n,), generator=g)
+    items = np.stack([b.numpy(), np.zeros(n, dtype=np.int64), h.numpy()], 1)
+    # always include the longest and the shortest request
+    lens = p.meta["lens"]
+    extra = [[int(np.argmax(lens)), 0, 0], [int(np.argmin(lens)), 0, p.Hq - 1]]
+    items = np.concatenate([items, np.array(extra)], 0)
+    ref = oracle.attention_items(p, items)
+    sel = got[items[:, 0], items[:, 1], items[:, 2]]
+    compare(sel, ref, what="c4 sampled")
+    assert dp.status() == 0
+
+
+def test_graph_replay_changing_lengths():
+    p = _problem("c3_64k")
+    dp = _dp(p)
+    L = p.max_kv_len
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dp.run()  # warm up (kernel attributes) outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        dp.run()
+    for q_live in (8, 5, 0, 8):
+        rl = torch.tensor([causal_row_len(L, 8, q_live)], dtype=torch.int32)
+        dp.row_len.copy_(rl)
+        dp.out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = dp.out.float().cpu().numpy()
+        ref = oracle.attention(p, row_len=rl)
+        compare(got, ref, what=f"replay q_live={q_live}")
+        if q_live == 0:
+            assert np.all(got == 0.0) and not np.signbit(got).any()
+    # bitwise determinism over repeated replays
+    first = dp.out.clone()
+    for _ in range(100):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), dp.out.view(torch.int16))
+
+
+def test_dead_rows_and_partial_rows():
+    p = make_dense(B=3, q=4, Hq=8, Hkv=2, D=128, page_size=16, lens=[100, 0, 37], seed=41,
+                   row_len=[[0, 98, 99, 100], [0, 0, 0, 0], [37, 0, 1, 36]])
+    got = _run(_dp(p))
+    ref = oracle.attention(p)
+    compare(got, ref, what="dead rows")
+    assert np.all(got[1] == 0) and np.all(got[0, 0] == 0)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("q,Hq,Hkv", [(1, 4, 1), (3, 8, 2), (16, 8, 1), (5, 24, 2)])
+def test_shapes_dense(D, q, Hq, Hkv):
+    p = make_dense(B=2, q=q, Hq=Hq, Hkv=Hkv, D=D, page_size=7, lens=[300, 77], seed=D + q + Hq)
+    got = _run(_dp(p))
+    compare(got, oracle.attention(p), what=f"D={D} q={q} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("q,Hq,Hkv", [(1, 4, 1), (4, 24, 2), (8, 8, 4)])
+def test_shapes_sparse(D, q, Hq, Hkv):
+    p = make_sparse(B=2, q=q, Hq=Hq, Hkv=Hkv, D=D, L=2000, topk_blocks=40, seed=D * 3 + q)
+    got = _run(_dp(p))
+    compare(got, oracle.attention(p), what=f"sparse D={D} q={q}")
+
+
+def test_device_scales():
+    p = _problem("c2")
+    got = _run(_dp(p, device_scales=True))
+    compare(got, _ref("c2"), what="device scales")
+
+
+def test_interleaved_kv_strides():
+    p = make_dense(B=2, q=2, Hq=4, Hkv=2, D=128, page_size=16, lens=[500, 260], seed=43)
+    nb, P, H, D = p.k_cache.shape
+    kv = torch.empty((nb, P, 2, H, D), dtype=torch.uint8)
+    kv[:, :, 0] = p.k_cache
+    kv[:, :, 1] = p.v_cache
+    kvd = kv.cuda()
+    dp = _dp(p, k_cache=kvd[:, :, 0], v_cache=kvd[:, :, 1])
+    got = _run(dp)
+    compare(got, oracle.attention(p), what="interleaved K/V")
+
+
+def test_out_of_range_block_sets_status():
+    p = make_dense(B=1, q=2, Hq=2, Hkv=1, D=64, page_size=16, lens=[200], seed=44)
+    dp = _dp(p)
+    bad = dp.block_table.clone()
+    bad[0, 3] = p.k_cache.shape[0] + 5
+    dp.block_table.copy_(bad)
+    got = _run(dp)
+    assert np.isfinite(got).all()
+    assert dp.status() & 0x1
+
+
+def test_length_above_bound_sets_status():
+    p = make_dense(B=1, q=2, Hq=2, Hkv=1, D=64, page_size=16, lens=[200], seed=45)
+    dp = _dp(p)
+    dp.row_len.fill_(10_000)
+    got = _run(dp)
+    assert np.isfinite(got).all()
+    assert dp.status() & 0x2
+    # clamped to the planned bound: every row then sees all 200 tokens
+    rl = torch.full((1, 2), 200, dtype=torch.int32)
+    compare(got, oracle.attention(p, row_len=rl), what="clamped lengths")
+
+
+def test_sparse_bad_microblock_sets_status():
+    p = make_sparse(B=1, q=2, Hq=2, Hkv=1, D=64, L=400, topk_blocks=8, seed=46)
+    dp = _dp(p)
+    t = dp.entry_tbl.clone()
+    t[0, 0] = p.k_cache.shape[0] + 1
+    dp.entry_tbl.copy_(t)
+    got = _run(dp)
+    assert np.isfinite(got).all()
+    assert dp.status() & 0x1
+
+
+def test_batch_zero_is_noop():
+    from fp8_e4m3_paged_gb300 import binding as B
+
+    d = B.make_desc(mode=0, batch=0, q_max=1, num_q_heads=1, num_kv_heads=1, head_dim=64,
+                    page_size=16, max_kv_len=0, max_blocks=0, num_kv_blocks=1)
+    plan = B.fp8kv_attn_plan(d)
+    ws = torch.zeros(int(plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    a = B.Args()
+    a.workspace = ws.data_ptr()
+    a.workspace_bytes = ws.numel()
+    B.fp8kv_attn_split(plan, a, torch.cuda.current_stream().cuda_stream)
+    B.fp8kv_attn_combine(plan, a, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
