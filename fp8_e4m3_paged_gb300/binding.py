@@ -26,6 +26,10 @@ ECUDA = -5
 MODE_DENSE = 0
 MODE_SPARSE_PAGE4 = 1
 
+KERNEL_AUTO = 0
+KERNEL_GENERIC = 1
+KERNEL_TC = 2
+
 STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LEN = 0x2
 STATUS_BAD_ENTRIES = 0x4
@@ -35,7 +39,7 @@ STATUS_TIMEOUT = 0x8
 class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "batch", "q_max", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
-        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits")]
+        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits", "kernel")]
 
 
 class Plan(ctypes.Structure):
@@ -126,9 +130,9 @@ def fp8kv_attn_combine(plan: Plan, args: Args, stream: int = 0) -> None:
 
 def make_desc(*, mode: int, batch: int, q_max: int, num_q_heads: int, num_kv_heads: int,
               head_dim: int, page_size: int, max_kv_len: int, max_blocks: int,
-              num_kv_blocks: int, num_sms: int = 0, num_splits: int = 0) -> Desc:
+              num_kv_blocks: int, num_sms: int = 0, num_splits: int = 0, kernel: int = 0) -> Desc:
     return Desc(mode, batch, q_max, num_q_heads, num_kv_heads, head_dim, page_size,
-                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits)
+                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits, kernel)
 
 
 def _ptr(t) -> Optional[int]:

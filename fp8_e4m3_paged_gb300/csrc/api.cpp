@@ -45,6 +45,8 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   if (d->page_size < 1 || d->max_kv_len < 0 || d->max_blocks < 0 || d->num_kv_blocks < 1)
     return FP8KV_EINVAL;
   if (d->num_sms < 0 || d->num_splits < 0) return FP8KV_EINVAL;
+  if (d->kernel < FP8KV_KERNEL_AUTO || d->kernel > FP8KV_KERNEL_TC) return FP8KV_EINVAL;
+  if (d->kernel == FP8KV_KERNEL_TC && d->head_dim != 128 && d->head_dim != 256) return FP8KV_EUNSUPPORTED;
   if (d->mode == FP8KV_MODE_DENSE) {
     if ((int64_t)d->max_blocks * d->page_size < d->max_kv_len) return FP8KV_EINVAL;
   } else {
@@ -77,26 +79,48 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   P.rows = d->q_max * P.group;
   P.num_sms = sms;
 
-  // Generic CUDA-core path.
-  P.kernel = kGeneric;
-  P.row_chunk = P.rows < kMaxRowChunk ? P.rows : kMaxRowChunk;
+  // Kernel choice: the tcgen05 path when the grouped rows fill at least a
+  // quarter of its 64-row MMA tile and D is 128 or 256; otherwise the generic
+  // FP32 CUDA-core path (few rows per KV head: decode, small groups).
+  const bool tc = d->kernel == FP8KV_KERNEL_TC ||
+                  (d->kernel == FP8KV_KERNEL_AUTO && (P.head_dim == 128 || P.head_dim == 256) && P.rows >= 16);
+  int tile, ctas_per_sm, max_part_tiles;
+  if (tc) {
+    P.kernel = kTc;
+    P.row_chunk = P.rows < kTcRows ? P.rows : kTcRows;
+    tile = kTcTileTokens;
+    P.block_threads = kTcThreads;
+    P.smem_bytes = tc_smem_bytes(P.head_dim);
+    ctas_per_sm = 1;
+    max_part_tiles = kTcMaxPartTiles;
+  } else {
+    P.kernel = kGeneric;
+    P.row_chunk = P.rows < kMaxRowChunk ? P.rows : kMaxRowChunk;
+    tile = kGenericTileTokens;
+    P.block_threads = kGenericThreads;
+    P.smem_bytes = generic_smem_bytes(P.head_dim, P.row_chunk);
+    ctas_per_sm = 2;
+    max_part_tiles = kGenericMaxPartTiles;
+  }
   const int n_chunks = ceil_div(P.rows, P.row_chunk);
-  P.tile_tokens = kGenericTileTokens;
-  P.block_threads = kGenericThreads;
-  P.smem_bytes = generic_smem_bytes(P.head_dim, P.row_chunk);
+  P.tile_tokens = tile;
 
-  // Split count: enough CTAs for about two waves, never more partitions than
-  // tiles of work (dense: tokens / 32, sparse: entries / 8).
+  // Split count: about one wave of CTAs (two for the generic path), never
+  // more partitions than tiles of work (dense: tokens / tile, sparse: entries
+  // / (tile / 4)), and partitions capped in length because FP32 accumulation
+  // error grows with the number of tiles one partition sums.
   const int64_t units = (int64_t)d->batch * d->num_kv_heads * n_chunks;
   const int max_tiles = d->mode == FP8KV_MODE_DENSE
-                            ? (d->max_kv_len > 0 ? ceil_div(d->max_kv_len, kGenericTileTokens) : 1)
-                            : (d->max_blocks > 0 ? ceil_div(d->max_blocks, kGenericTileTokens / 4) : 1);
+                            ? (d->max_kv_len > 0 ? ceil_div(d->max_kv_len, tile) : 1)
+                            : (d->max_blocks > 0 ? ceil_div(d->max_blocks, tile / 4) : 1);
   int S;
   if (d->num_splits > 0) {
     S = d->num_splits;
   } else {
-    const int64_t target = 2LL * sms;
+    const int64_t target = (int64_t)ctas_per_sm * sms;
     S = units > 0 ? ceil_div(target, units) : 1;
+    const int by_len = ceil_div(max_tiles, max_part_tiles);
+    if (S < by_len) S = by_len;
     if (S > max_tiles) S = max_tiles;
     if (S < 1) S = 1;
   }

@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
     for (int s = 0; s < p.S; ++s) {
       const float2 v = ml[s * sstride];
       if (v.y > 0.f) {
-        const float w = fast_exp2(v.x - M);
+        const float w = exp2_int(v.x - M);  // maxima are integers: exact
         L = fmaf(w, v.y, L);
         const float* a = acc + (int64_t)s * sstride * D;
 #pragma unroll

@@ -47,6 +47,22 @@ __device__ __forceinline__ void set_status(unsigned int* status, unsigned int bi
   atomicOr(status, bit);
 }
 
+// hi + lo += x without rounding loss in the hi/lo pair (Knuth's TwoSum: the
+// rounding error of hi + x is recovered exactly and folded into lo).
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bp = __fsub_rn(s, hi);
+  const float ap = __fsub_rn(s, bp);
+  const float err = __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(x, bp));
+  hi = s;
+  lo = __fadd_rn(lo, err);
+}
+
+// 2^x for an integer-valued x <= 0 (running maxima are kept integral), exact.
+__device__ __forceinline__ float exp2_int(float x) {
+  return x < -200.f ? 0.f : ldexpf(1.0f, (int)x);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -12,13 +12,14 @@ namespace fp8kv {
 
 // Split-kernel variants a plan may choose.
 enum Kernel : int32_t {
-  kGeneric = 0,  // CUDA-core FP32 path, any supported shape
-  kTc = 1,       // tcgen05 tensor-core path (dense and sparse, rows <= 64)
+  kGeneric = FP8KV_KERNEL_GENERIC,  // CUDA-core FP32 path, any supported shape
+  kTc = FP8KV_KERNEL_TC,            // tcgen05 tensor-core path (head_dim 128/256)
 };
 
 constexpr int kGenericThreads = 256;
 constexpr int kGenericTileTokens = 32;  // tokens (dense) or 8 entries (sparse)
 constexpr int kMaxRowChunk = 64;        // query vectors per split CTA
+constexpr int kGenericMaxPartTiles = 32; // longest partition of the generic path (tiles)
 
 // Everything a split or combine kernel needs, resolved on the host.
 struct Params {
@@ -72,5 +73,12 @@ struct DeviceOnce {
 
 // Shared-memory bytes of the generic split kernel for a head dim and row chunk.
 int generic_smem_bytes(int D, int row_chunk);
+
+// Tensor-core path: shared-memory bytes (D = 128 or 256), threads, tile size.
+int tc_smem_bytes(int D);
+constexpr int kTcThreads = 288;
+constexpr int kTcTileTokens = 64;
+constexpr int kTcRows = 64;
+constexpr int kTcMaxPartTiles = 32;  // longest partition of the tensor-core path (tiles)
 
 }  // namespace fp8kv

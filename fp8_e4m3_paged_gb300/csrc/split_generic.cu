@@ -6,7 +6,7 @@
 // (dense) or 8 four-token microblocks (sparse) with 16-byte loads, decodes the
 // bytes exactly to FP32, and runs the online softmax with FP32 state:
 //   s = (q . k) * softmax_scale * k_scale * log2(e)
-//   m' = max(m, max_tile s);  acc = acc * 2^(m - m') + sum_t 2^(s_t - m') v_t
+//   m' = max(m, ceil(max_tile s));  acc = acc * 2^(m - m') + sum_t 2^(s_t - m') v_t
 //   l  = l * 2^(m - m') + sum_t 2^(s_t - m')
 // and finally stores the unnormalised FP32 numerators acc with (m, l)
 // ("DFlash2 E4M3 attention with FP32 state", intro paragraph 4: FP32
@@ -214,17 +214,32 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
     __syncthreads();
 
     // ------------------------------------------------------ scores (lane = token)
+    // Compensated QK: products q*k are exact in FP32 (11-bit x 4-bit
+    // significands); they are summed in chunks of 8 and the chunk sums are
+    // combined with an error-free TwoSum into hi + lo, so the logit keeps
+    // more than FP32 precision.  The base-2 exponent is then formed as
+    // fma(hi, c, -m) + lo*c, which rounds only the small difference to the
+    // running max ("DFlash2 E4M3 attention with FP32 state", intro paragraph
+    // 4: compensated QK accumulation).
     {
-      float dot[RPW];
+      float hi[RPW], lo[RPW];
 #pragma unroll
-      for (int k = 0; k < RPW; ++k) dot[k] = 0.f;
+      for (int k = 0; k < RPW; ++k) { hi[k] = 0.f; lo[k] = 0.f; }
       const float* kr = Ks + lane * (D + 1);
       const float* qr = Qs + warp * RPW;
-#pragma unroll 4
-      for (int d = 0; d < D; ++d) {
-        const float kv = kr[d];
+#pragma unroll 1
+      for (int d0 = 0; d0 < D; d0 += 8) {
+        float ch[RPW];
 #pragma unroll
-        for (int k = 0; k < RPW; ++k) dot[k] = fmaf(qr[d * RCMAX + k], kv, dot[k]);
+        for (int k = 0; k < RPW; ++k) ch[k] = 0.f;
+#pragma unroll
+        for (int d = d0; d < d0 + 8; ++d) {
+          const float kv = kr[d];
+#pragma unroll
+          for (int k = 0; k < RPW; ++k) ch[k] = fmaf(qr[d * RCMAX + k], kv, ch[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < RPW; ++k) two_sum_acc(hi[k], lo[k], ch[k]);
       }
       const int t = lane;
       const int tok = tb + ((MODE == FP8KV_MODE_DENSE) ? t : t / 4);
@@ -238,14 +253,17 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
           vis = (n >= 0) && (tok < u1) && (tok < n);
         else
           vis = (n >= 0) && (tok < u1) && ((mk >> (4 * n + (t & 3))) & 1u);
-        const float sv = vis ? dot[k] * c : -INFINITY;
+        const float sv = vis ? fmaf(hi[k], c, lo[k] * c) : -INFINITY;
         float mt = sv;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-        const float m_new = fmaxf(m_run[k], mt);
+        // integer-valued running max: rescale factors 2^(m - m') and the
+        // combine's partition weights are then exact powers of two
+        const float m_new = fmaxf(m_run[k], ceilf(mt));
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float pv = vis ? fast_exp2(sv - m_use) : 0.f;
-        const float alpha = (m_run[k] == -INFINITY) ? 0.f : fast_exp2(m_run[k] - m_use);
+        const float arg = fmaf(lo[k], c, fmaf(hi[k], c, -m_use));
+        const float pv = vis ? exp2f(arg) : 0.f;
+        const float alpha = (m_run[k] == -INFINITY) ? 0.f : exp2_int(m_run[k] - m_use);
         float ps = pv;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);

@@ -82,6 +82,11 @@ extern "C" {
 #define FP8KV_MODE_DENSE 0
 #define FP8KV_MODE_SPARSE_PAGE4 1
 
+/* Split-kernel choice (desc.kernel; the plan records the one chosen). */
+#define FP8KV_KERNEL_AUTO 0
+#define FP8KV_KERNEL_GENERIC 1 /* FP32 CUDA-core path: every supported shape */
+#define FP8KV_KERNEL_TC 2      /* tcgen05 tensor-core path: head_dim 128/256 (else FP8KV_EUNSUPPORTED) */
+
 /* Sticky device status bits (workspace word at byte offset 0). */
 #define FP8KV_STATUS_BAD_BLOCK 0x1   /* block / microblock id outside [0, num_kv_blocks) */
 #define FP8KV_STATUS_BAD_LEN 0x2     /* a row length < 0 or > max_kv_len (clamped) */
@@ -106,6 +111,7 @@ typedef struct {
   int32_t num_kv_blocks; /* physical blocks in the page pool (for bounds checks), >= 1 */
   int32_t num_sms;       /* SMs to plan for; 0 = ask the current device */
   int32_t num_splits;    /* split-KV partitions per (request, KV head); 0 = planner's choice */
+  int32_t kernel;        /* FP8KV_KERNEL_*: 0 = planner's choice */
 } fp8kv_attn_desc;
 
 /* A plan: plain data, owned by the caller, nothing to free.  Fields other than
@@ -118,7 +124,7 @@ typedef struct {
   int32_t rows;          /* q_max * group: query vectors per (request, KV head) */
   int32_t num_splits;    /* S */
   int32_t tile_tokens;   /* tokens per pipeline tile (dense) */
-  int32_t kernel;        /* split-kernel variant chosen */
+  int32_t kernel;        /* FP8KV_KERNEL_GENERIC or FP8KV_KERNEL_TC */
   int32_t grid[3];       /* split-kernel grid */
   int32_t block_threads; /* split-kernel block size */
   int32_t smem_bytes;    /* split-kernel dynamic shared memory */

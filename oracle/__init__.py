@@ -16,6 +16,8 @@ Parity status of each exported function (what pins it, in ``tests/``):
                       all-visible sparse == dense causal), planted mistakes
   attention_split     equals attention within 1e-13 (split-count invariance)
   row_weights         sum to 1, two-token logistic closed form
+  attention_abs       equals attention when every V byte is non-negative;
+                      bounds |attention| elementwise
 """
 
 from __future__ import annotations
@@ -88,6 +90,7 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.orc_attention.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_items.argtypes = [P, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_split.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_attention_abs.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
     lib.orc_row_weights.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     _libs[plant] = lib
     return lib
@@ -174,6 +177,16 @@ def attention_items(p, items, threads: Optional[int] = None, plant: int = 0, **o
                                          out.ctypes.data, threads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected the problem or an item")
+    return out
+
+
+def attention_abs(p, threads: Optional[int] = None, plant: int = 0, **over) -> np.ndarray:
+    """Per-element condition v_scale * sum_j w_j |dec(V_j[d])| ([B][q][Hq][D])."""
+    pin = _Pinned(p, **over)
+    out = np.zeros((p.B, p.q, p.Hq, p.D), dtype=np.float64)
+    rc = load(plant).orc_attention_abs(ctypes.byref(pin.s), out.ctypes.data, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
     return out
 
 

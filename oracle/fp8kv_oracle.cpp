@@ -198,6 +198,30 @@ ORC_API int orc_row_weights(const orc_problem* p, int b, int r, int h, double* w
   return n;
 }
 
+// Condition of each output element: v_scale * sum_j w_j |dec(V_j[d])|, the
+// magnitude an FP32 evaluation's rounding errors scale with (a forward error
+// bound for a weighted sum is proportional to the sum of |terms|).
+static void row_head_abs(const orc_problem* p, int b, int r, int h, double* out) {
+  const int D = p->D;
+  std::vector<Tok> toks;
+  visible(p, b, r, group_of(p, h), toks);
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  if (toks.empty()) return;
+  std::vector<double> z;
+  logits(p, b, r, h, toks, z);
+  double M = -std::numeric_limits<double>::infinity();
+  for (double v : z) M = std::max(M, v);
+  double S = 0.0;
+  for (double v : z) S += std::exp(v - M);
+  std::vector<double> acc(D, 0.0);
+  for (size_t j = 0; j < toks.size(); ++j) {
+    const double w = std::exp(z[j] - M) / S;
+    const uint8_t* vb = p->v_cache + toks[j].v_off;
+    for (int d = 0; d < D; ++d) acc[d] += w * std::fabs(orc_e4m3(vb[d]));
+  }
+  for (int d = 0; d < D; ++d) out[d] = std::fabs(p->v_scale) * acc[d];
+}
+
 static void row_head(const orc_problem* p, int b, int r, int h, double* out) {
   const int D = p->D;
   std::vector<Tok> toks;
@@ -316,6 +340,19 @@ ORC_API int orc_attention_items(const orc_problem* p, const int32_t* items, int 
   }
   parallel_items(n_items, nthreads, [&](int64_t i) {
     row_head(p, items[3 * i], items[3 * i + 1], items[3 * i + 2], out + i * p->D);
+  });
+  return 0;
+}
+
+// out: [B][q][Hq][D] doubles, v_scale * sum_j w_j |dec(V_j[d])|.
+ORC_API int orc_attention_abs(const orc_problem* p, double* out, int nthreads) {
+  if (check(p)) return -1;
+  const int64_t n = (int64_t)p->B * p->q * p->Hq;
+  parallel_items(n, nthreads, [&](int64_t i) {
+    const int h = (int)(i % p->Hq);
+    const int r = (int)((i / p->Hq) % p->q);
+    const int b = (int)(i / ((int64_t)p->Hq * p->q));
+    row_head_abs(p, b, r, h, out + i * p->D);
   });
   return 0;
 }

@@ -6,8 +6,10 @@ the finite range), page-pool layout with a seeded block permutation, poisoned
 unused slots, causal live lengths and the QSA microblock selection.  No
 attention arithmetic lives here.
 
-Workload recipes (all on the CPU with ``torch.Generator``; seeds 101..105 for
-the five named configurations are a free choice of this project):
+Workload recipes (all on the CPU; Gaussian and outlier draws come from
+numpy's PCG64 so that x86 and Arm hosts build identical bytes, permutations
+and uniform draws from a seeded ``torch.Generator``; seeds 101..105 for the
+five named configurations are a free choice of this project):
 
 * ``c1``  one request, q=2 verify rows, Hq=6/Hkv=1, D=256, context 1024,
   page size 16, 64 pages randomly permuted; K,V ~ N(0,1) quantised with a
@@ -105,12 +107,16 @@ class Problem:
 # primitives
 # --------------------------------------------------------------------------
 
-def _gen(seed: int, *salt: int) -> torch.Generator:
-    g = torch.Generator()
+def _seed(seed: int, *salt: int) -> int:
     h = seed
     for s in salt:
         h = (h * 1_000_003 + s + 7) % (2**62)
-    g.manual_seed(h)
+    return h
+
+
+def _gen(seed: int, *salt: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(_seed(seed, *salt))
     return g
 
 
@@ -120,10 +126,16 @@ def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
     return y.to(torch.float8_e4m3fn).view(torch.uint8)
 
 
-def _gauss(gen: torch.Generator, shape, outliers: bool) -> torch.Tensor:
-    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+def _gauss(key: int, shape, outliers: bool) -> torch.Tensor:
+    """N(0,1) float32 draws from numpy's PCG64 generator, which gives the
+    same values on x86 and Arm hosts (torch's vectorised CPU normal sampler
+    does not), so every machine builds byte-identical caches."""
+    import numpy as np
+
+    rng = np.random.Generator(np.random.PCG64(key))
+    x = torch.from_numpy(rng.standard_normal(size=tuple(shape), dtype=np.float32))
     if outliers:
-        sel = torch.rand(shape, generator=gen) < 0.01
+        sel = torch.from_numpy(rng.random(size=tuple(shape), dtype=np.float32) < 0.01)
         x[sel] *= 20.0
     return x
 
@@ -194,7 +206,7 @@ def make_dense(
     v_cache = torch.full((num_blocks, page_size, Hkv, D), poison, dtype=torch.uint8)
 
     def draw(b, which):
-        return _gauss(_gen(seed, 2, b, which), (lens[b], Hkv, D), outliers)
+        return _gauss(_seed(seed, 2, b, which), (lens[b], Hkv, D), outliers)
 
     if value_mode == "per_tensor":
         kmax = 0.0
@@ -231,8 +243,7 @@ def make_dense(
             k_cache[pid, :rem] = kb[full * page_size:]
             v_cache[pid, :rem] = vb[full * page_size:]
 
-    qv = torch.randn((B, q, Hq, D), generator=_gen(seed, 3), dtype=torch.float32)
-    q_fp16 = qv.to(torch.float16)
+    q_fp16 = _gauss(_seed(seed, 3), (B, q, Hq, D), False).to(torch.float16)
 
     if row_len is None:
         rl = torch.tensor([causal_row_len(lens[b], q) for b in range(B)], dtype=torch.int32)
@@ -288,7 +299,7 @@ def make_sparse(
     v_cache[0] = poison
 
     def draw(b, which):
-        return _gauss(_gen(seed, 12, b, which), (nmb * P, Hkv, D), outliers)
+        return _gauss(_seed(seed, 12, b, which), (nmb * P, Hkv, D), outliers)
 
     kmax = max(float(draw(b, 0).abs().max()) for b in range(B))
     vmax = max(float(draw(b, 1).abs().max()) for b in range(B))
@@ -339,10 +350,10 @@ def make_sparse(
         n_entries[b] = n
     entry_mask = _u32_bits(entry_mask)
 
-    qv = torch.randn((B, q, Hq, D), generator=_gen(seed, 14), dtype=torch.float32)
+    q16 = _gauss(_seed(seed, 14), (B, q, Hq, D), False).to(torch.float16)
     return Problem(
         name=name, mode="sparse", B=B, q=q, Hq=Hq, Hkv=Hkv, D=D, page_size=P,
-        q_fp16=qv.to(torch.float16), k_cache=k_cache, v_cache=v_cache,
+        q_fp16=q16, k_cache=k_cache, v_cache=v_cache,
         softmax_scale=float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
         k_scale=float(ks), v_scale=float(vs), max_kv_len=L,
         entry_tbl=entry_tbl, entry_mask=entry_mask, n_entries=n_entries,

@@ -4,12 +4,24 @@ Per output tensor: relative L2 <= 5e-4 (all exact zeros when the reference is
 all zero), every element within 4 fp16 ulps of the reference value, where
 ulp16(x) = 2^(max(floor(log2|x|), -14) - 10) (2^-24 at and below the fp16
 subnormal range), and no NaN or Inf.
+
+FP32 floor (only where a caller passes ``cond``): an output element that
+cancels to a value far below the magnitude of its terms cannot be resolved by
+any FP32-state evaluation to 4 fp16 ulps of the (tiny) result.  For such
+elements the per-element bound becomes
+    4 ulp16(ref) + COND_U32 * 2^-24 * cond,
+cond = v_scale * sum_j w_j |V_j[d]| (the oracle's attention_abs), i.e. the
+standard forward error bound of a weighted sum evaluated with unit roundoff
+2^-24, with COND_U32 roundings (exponent, probability split, PV accumulation,
+partition combine, normalisation).  Where cond ~ |ref| the extra term is
+below 0.01 fp16 ulp, so the strict bound is unchanged there.
 """
 
 import numpy as np
 
 REL_L2 = 5e-4
 MAX_ULPS = 4.0
+COND_U32 = 16.0
 
 
 def ulp16(ref: np.ndarray) -> np.ndarray:
@@ -20,7 +32,7 @@ def ulp16(ref: np.ndarray) -> np.ndarray:
     return np.exp2(np.maximum(e, -14.0) - 10.0)
 
 
-def compare(gpu, ref, *, what="output"):
+def compare(gpu, ref, *, what="output", cond=None):
     g = np.asarray(gpu, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     assert g.shape == r.shape, (g.shape, r.shape)
@@ -39,7 +51,16 @@ def compare(gpu, ref, *, what="output"):
     ulps = np.abs(diff) / u
     stats["max_ulps"] = float(ulps.max()) if ulps.size else 0.0
     assert stats["rel_l2"] <= REL_L2, f"{what}: rel L2 {stats['rel_l2']:.3e} > {REL_L2}"
-    if stats["max_ulps"] > MAX_ULPS:
-        i = np.unravel_index(np.argmax(ulps), ulps.shape)
-        raise AssertionError(f"{what}: {stats['max_ulps']:.2f} fp16 ulps at {i}: gpu {g[i]!r} ref {r[i]!r}")
+    if cond is None:
+        bound = MAX_ULPS * u
+    else:
+        c = np.asarray(cond, dtype=np.float64)
+        bound = MAX_ULPS * u + COND_U32 * 2.0 ** -24 * c
+        stats["max_frac_of_bound"] = float((np.abs(diff) / bound).max()) if diff.size else 0.0
+    bad = np.abs(diff) > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.abs(diff) / bound), diff.shape)
+        extra = "" if cond is None else f" cond {float(np.asarray(cond)[i]):.3e}"
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of bound; worst {ulps[i]:.2f} fp16 ulps "
+                             f"at {i}: gpu {g[i]!r} ref {r[i]!r}{extra}")
     return stats

@@ -77,7 +77,7 @@ def test_dense_tiny_exact(orc, seed):
                    row_len=[[5, 6, 7], [0, 4, 5]], k_scale=None)
     got = orc.attention(p)
     ref = _exact_dense(p)
-    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-15)
     assert np.all(got[1, 0] == 0.0)
 
 
@@ -85,7 +85,7 @@ def test_dense_tiny_exact(orc, seed):
 def test_dense_tiny_direct_scales(orc, seed):
     p = make_dense(B=1, q=2, Hq=3, Hkv=1, D=3, page_size=2, lens=[8], seed=seed,
                    value_mode="direct", k_scale=0.37, v_scale=1.9, softmax_scale=0.7)
-    np.testing.assert_allclose(orc.attention(p), _exact_dense(p), rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(orc.attention(p), _exact_dense(p), rtol=1e-13, atol=1e-15)
 
 
 @pytest.mark.parametrize("seed", [6, 7])
@@ -93,5 +93,5 @@ def test_sparse_tiny_exact(orc, seed):
     p = make_sparse(B=2, q=3, Hq=4, Hkv=2, D=2, L=23, topk_blocks=3, seed=seed)
     got = orc.attention(p)
     ref = _exact_sparse(p)
-    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-15)
     assert np.isfinite(got).all()

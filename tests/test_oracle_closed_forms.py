@@ -92,3 +92,14 @@ def test_scale_roles(orc):
     p3 = make_dense(B=1, q=2, Hq=2, Hkv=1, D=16, page_size=8, lens=[40], seed=16,
                     value_mode="direct", k_scale=0.74, v_scale=1.9, softmax_scale=0.25)
     assert np.abs(orc.attention(p3) - a).max() > 1e-3
+
+
+def test_abs_condition(orc):
+    p = make_dense(B=1, q=3, Hq=2, Hkv=1, D=32, page_size=8, lens=[90], seed=17)
+    out = orc.attention(p)
+    ab = orc.attention_abs(p)
+    assert np.all(ab >= np.abs(out) * (1 - 1e-12))
+    # with every V byte non-negative the two coincide exactly
+    p.v_cache &= 0x7F
+    p.v_cache[p.v_cache == 0x7F] = 0x7E
+    assert np.array_equal(orc.attention_abs(p), orc.attention(p))
