@@ -5,10 +5,15 @@
 //
 // written as fp16 with round-to-nearest-even.  A query vector whose total L is
 // 0 (dead row, or nothing visible) gets +0.0.  Partitions with l_s = 0 are
-// skipped by a branch, so their numerators are never read ("DFlash2 E4M3
-// attention with FP32 state", intro paragraph 4: FP32 combination, FP16 final
-// activation; "Qwen4Exp: fp8_e4m3 main KV cache on the QSA path", review:
-// v_scale acts as the output scale).
+// skipped by a branch, so their numerators are never read.  The partition
+// maxima are integers (base-2 units), so every w_s is an exact power of two
+// ("DFlash2 E4M3 attention with FP32 state", intro paragraph 4: FP32
+// combination, FP16 final activation; "Qwen4Exp: fp8_e4m3 main KV cache on
+// the QSA path", review: v_scale acts as the output scale).
+//
+// One CTA per (query vector, 64-wide slice of D); its 256 threads are 16
+// partition lanes x 16 float4 columns, so the partitions of one vector are
+// read in parallel and reduced in shared memory in a fixed order.
 #include <cstdint>
 
 #include <cuda_fp16.h>
@@ -20,71 +25,109 @@
 namespace fp8kv {
 namespace {
 
-constexpr int CT = 128;  // threads per combine CTA
+constexpr int CT = 256;
+constexpr int SL = 16;    // partition lanes
+constexpr int DW = 64;    // d slice per CTA
+constexpr int MAXS = 1024;  // partitions staged in shared memory per pass
 
-// One CTA per output vector (b, r, h); thread handles d = tid + k*CT.
-template <int D>
 __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
-  constexpr int PER = (D + CT - 1) / CT;
-  const int idx = blockIdx.x;  // (b*q_max + r)*Hq + h
+  __shared__ float red_m[CT / 32];
+  __shared__ float s_w[MAXS];       // weight 2^(m_s - M) of live partitions (0 = dead)
+  __shared__ float s_l[MAXS];
+  __shared__ float4 red_o[SL][DW / 4];
+  __shared__ float red_l[SL];
+  const int D = p.D;
+  const int n_slices = D / DW;
+  const int idx = blockIdx.x / n_slices;  // (b*q_max + r)*Hq + h
+  const int slice = blockIdx.x % n_slices;
   const int h = idx % p.Hq;
   const int r = (idx / p.Hq) % p.q_max;
   const int b = idx / (p.Hq * p.q_max);
   const int g = h / p.G;
   const int i = r * p.G + (h % p.G);
   const int64_t base = (((int64_t)b * p.Hkv + g) * p.S) * p.rows + i;
-  const float2* ml = p.ml + base;
-  const float* acc = p.partial + base * D;
-  const int64_t sstride = p.rows;  // partitions of one query vector are rows apart
+  const float2* ml = p.ml + base;           // partition s at ml[s * rows]
+  const int64_t sstride = p.rows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // global max over live partitions (all (m, l) pairs read in parallel)
   float M = -INFINITY;
-  for (int s = 0; s < p.S; ++s) {
+  for (int s = tid; s < p.S; s += CT) {
     const float2 v = ml[s * sstride];
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = red_m[0];
+#pragma unroll
+  for (int k = 1; k < CT / 32; ++k) M = fmaxf(M, red_m[k]);
+
+  const int sl = tid / (DW / 4), c4 = tid % (DW / 4);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  float o[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) o[k] = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < p.S; ++s) {
-      const float2 v = ml[s * sstride];
-      if (v.y > 0.f) {
-        const float w = exp2_int(v.x - M);  // maxima are integers: exact
-        L = fmaf(w, v.y, L);
-        const float* a = acc + (int64_t)s * sstride * D;
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const int d = threadIdx.x + k * CT;
-          if (d < D) o[k] = fmaf(w, a[d], o[k]);
-        }
+  const float* acc = p.partial + base * D + slice * DW + c4 * 4;
+  for (int s0 = 0; s0 < p.S && M != -INFINITY; s0 += MAXS) {
+    const int ns = min(MAXS, p.S - s0);
+    __syncthreads();
+    for (int k = tid; k < ns; k += CT) {
+      const float2 v = ml[(s0 + k) * sstride];
+      const bool live = v.y > 0.f;
+      s_w[k] = live ? exp2_int(v.x - M) : 0.f;  // integer maxima: exact
+      s_l[k] = live ? v.y : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = sl; k < ns; k += SL) {
+      const float w = s_w[k];
+      if (w != 0.f) {  // dead partitions' numerators are never read
+        const float4 a = *reinterpret_cast<const float4*>(acc + (int64_t)(s0 + k) * sstride * D);
+        o.x = fmaf(w, a.x, o.x);
+        o.y = fmaf(w, a.y, o.y);
+        o.z = fmaf(w, a.z, o.z);
+        o.w = fmaf(w, a.w, o.w);
+        L = fmaf(w, s_l[k], L);
       }
     }
   }
-  const float vs = p.v_scale_dev ? *p.v_scale_dev : p.v_scale;
-  const float f = (L > 0.f) ? vs / L : 0.f;
-  uint16_t* out = p.out + (int64_t)idx * D;
+  red_o[sl][c4] = o;
+  if (c4 == 0) red_l[sl] = L;
+  __syncthreads();
+  if (tid < DW / 4) {
+    float4 t = red_o[0][tid];
+    float Lt = red_l[0];
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int d = threadIdx.x + k * CT;
-    if (d < D) {
-      const float y = (L > 0.f) ? o[k] * f : 0.f;
-      out[d] = __half_as_ushort(__float2half_rn(y));
+    for (int k = 1; k < SL; ++k) {
+      const float4 u = red_o[k][tid];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+      Lt += red_l[k];
     }
+    const float vs = p.v_scale_dev ? *p.v_scale_dev : p.v_scale;
+    const float f = (Lt > 0.f) ? vs / Lt : 0.f;
+    const float y0 = (Lt > 0.f) ? t.x * f : 0.f;
+    const float y1 = (Lt > 0.f) ? t.y * f : 0.f;
+    const float y2 = (Lt > 0.f) ? t.z * f : 0.f;
+    const float y3 = (Lt > 0.f) ? t.w * f : 0.f;
+    const __half2 h01 = __floats2half2_rn(y0, y1);
+    const __half2 h23 = __floats2half2_rn(y2, y3);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+    pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+    *reinterpret_cast<uint2*>(p.out + (int64_t)idx * D + slice * DW + tid * 4) = pk;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t st) {
-  const int n = p.B * p.q_max * p.Hq;
+  const int64_t n = (int64_t)p.B * p.q_max * p.Hq * (p.D / DW);
   if (n == 0) return cudaSuccess;
-  switch (p.D) {
-    case 64: combine_kernel<64><<<n, CT, 0, st>>>(p); break;
-    case 128: combine_kernel<128><<<n, CT, 0, st>>>(p); break;
-    case 256: combine_kernel<256><<<n, CT, 0, st>>>(p); break;
-    default: return cudaErrorInvalidValue;
-  }
+  if (p.D % DW) return cudaErrorInvalidValue;
+  combine_kernel<<<(unsigned)n, CT, 0, st>>>(p);
   (void)plan;
   return cudaGetLastError();
 }

@@ -3,21 +3,26 @@
 //
 // Per CTA: one partition (a contiguous token range, or entry range in the
 // sparse microblock mode) of one (request, KV head, row chunk).  Warp roles:
-//   warps 0-3  softmax: read S from TMEM, online softmax with FP32 state,
-//              write P = P_hi + P_lo (two fp16 halves) to TMEM, rescale O when
-//              the running max jumps, final epilogue (FP32 partial to HBM);
-//   warps 4-7  loaders: 16-byte loads of E4M3 K/V bytes from the paged cache,
-//              exact decode to fp16 (value * 2^-8), stores into swizzled
-//              shared-memory tiles (a ring of kStages stages);
-//   warp 8     TMEM allocation and UMMA issue (one elected thread).
+//   warp 13      producer (one thread): bulk copies (cp.async.bulk) of the
+//                tile's E4M3 K/V rows from the paged cache into a ring of raw
+//                shared-memory stages, completion counted in bytes on an
+//                mbarrier; runs of tokens contiguous in a page move as one
+//                copy; tokens no query row may see are never copied;
+//   warps 4-11   decoders: raw E4M3 -> exact fp16 with the hardware
+//                e4m3x2 -> f16x2 conversion, into swizzled operand tiles (a
+//                second ring); tokens that were not copied become zeros;
+//   warp 12      TMEM allocation and UMMA issue (one elected thread);
+//   warps 0-3    softmax: read S from TMEM, online softmax with FP32 state,
+//                write P = P_hi + P_lo (two fp16 halves) back to TMEM in place
+//                of S, rescale O when the running max jumps, epilogue.
 // Per 64-token tile:
-//   QK:  S[64 x 64]  = Q[64 x D] . K^T   (M=64, fp16 x fp16 -> fp32, A and B
-//        from shared memory, K-major)
-//   PV:  O[128 x D] += [P_hi; P_lo][128 x 64] . V[64 x D]  (M=128, A from
-//        TMEM, B from shared memory MN-major).  Row r of P_hi sits in TMEM
-//        lane 32*(r/16) + r%16 and its P_lo twin 16 lanes further, so one MMA
-//        accumulates both halves of the probability split; the epilogue adds
-//        the two accumulator rows in FP32.
+//   QK:  S[128 x 64] = Q[128 x D] . K^T   (M=128, A = Q resident in TMEM,
+//        B = K tile from shared memory, K-major).  Query vector 16w+j
+//        (j < 16) sits in TMEM lane 32w+j; lanes 32w+16..31 are zero rows.
+//   PV:  O[128 x D] += P[128 x 64] . V[64 x D]  (M=128, A from TMEM, B = V
+//        tile MN-major).  P_hi of vector 16w+j sits in lane 32w+j and its
+//        P_lo twin in lane 32w+16+j, so one MMA accumulates both halves of
+//        the probability split; the epilogue adds the two accumulator rows.
 // The hi/lo split keeps probabilities to ~22 bits ("compensated
 // probabilities"); the FP32 partition numerator, max and sum follow the FP32
 // state contract ("DFlash2 E4M3 attention with FP32 state", intro paragraph
@@ -41,46 +46,58 @@ namespace {
 
 using namespace tc;
 
-constexpr int kT = 64;          // tokens per tile (16 microblocks in sparse mode)
-constexpr int kRows = 64;       // query vectors per CTA (QK M)
-constexpr int kThreads = 288;   // 4 softmax + 4 loader + 1 MMA warps
-constexpr float kTau = 8.0f;    // lazy-rescale threshold (base-2 units)
+constexpr int kT = 64;              // tokens per tile (16 microblocks in sparse mode)
+constexpr int kRows = 64;           // query vectors per CTA
+constexpr int kSoftmaxWarps = 4;
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = 32 * kDecWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + kDecWarps;   // 12
+constexpr int kProdWarp = kMmaWarp + 1;               // 13
+constexpr int kThreads = 32 * (kProdWarp + 1);        // 448
+constexpr float kTau = 8.0f;        // lazy-rescale threshold (base-2 units)
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kMaxStages = 4;
 
 template <int D>
 struct Cfg {
-  static constexpr int kStages = (D == 256) ? 3 : 4;
-  static constexpr int kQBytes = kRows * D * 2;            // Q tile (fp16, swizzled)
+  static constexpr int kStages = (D == 256) ? 2 : 3;       // fp16 operand stages
+  static constexpr int kRaw = (D == 256) ? 3 : 4;          // raw E4M3 stages
   static constexpr int kKVBytes = kT * D * 2;              // one K or V tile (fp16)
   static constexpr int kStageBytes = 2 * kKVBytes;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffStages = kQBytes;
-  static constexpr int kOffMeta = kOffStages + kStages * kStageBytes;
-  // meta: barriers, tmem slot, per-stage sparse masks, per-row lengths
+  static constexpr int kRawBytes = 2 * kT * D;             // raw K rows then raw V rows
+  static constexpr int kOffStages = 0;
+  static constexpr int kOffRaw = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffMeta = kOffRaw + kRaw * kRawBytes;
   static constexpr int kMetaBytes = 1024;
   static constexpr int kSmem = kOffMeta + kMetaBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;      // 2 x 64 columns
-  static constexpr uint32_t kColP = 128;    // 2 x 32 columns
+  static constexpr uint32_t kColQ = 0;      // D/2 columns (fp16 pairs)
+  static constexpr uint32_t kColS = 128;    // 2 x 64 columns; P(i) overwrites S(i)
   static constexpr uint32_t kColO = 256;    // D columns
+  static_assert(kStages <= kMaxStages && kRaw <= kMaxStages, "ring sizes");
 };
 
 struct Meta {
-  uint64_t kv_full[4];
-  uint64_t kv_empty[4];
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];
+  uint64_t raw_full[kMaxStages];
+  uint64_t raw_empty[kMaxStages];
   uint64_t s_full[2];
+  uint64_t pv_done[2];
   uint64_t p_ready;
-  uint64_t pv_done;
   uint32_t tmem;
   uint32_t pad;
-  uint32_t masks[4][16];   // sparse: entry masks of each stage's tile
-  int32_t nrow[kRows];     // dense: live length of each query vector; sparse: its query row
+  uint64_t valid[kMaxStages];           // per raw stage: tokens that were copied
+  uint32_t raw_masks[kMaxStages][16];   // sparse: entry masks of each raw stage's tile
+  uint32_t masks[kMaxStages][16];       // sparse: entry masks of each operand stage's tile
+  int32_t nrow[kRows];                  // dense: live length of each query vector; sparse: its query row
 };
 
 // ---------------------------------------------------------------- TMEM 16xNb
 
 // 16 lanes x 256 bits (8 columns) per repeat; thread t holds, per repeat g,
-// lanes (t/4) and (t/4 + 8), columns 8g + 2*(t%4) + {0, 1}.
+// lanes (t/4) and (t/4 + 8), columns 8g + 2*(t%4) + {0, 1}, registers in the
+// order (lane t/4: col, col+1), (lane t/4+8: col, col+1).
 __device__ __forceinline__ void ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
@@ -94,7 +111,7 @@ __device__ __forceinline__ void ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
 }
 
 // 16 lanes x 128 bits (4 columns) per repeat; thread t holds, per repeat g,
-// lane (t/4) column 4g + t%4, and lane (t/4 + 8) column 4g + t%4.
+// lane (t/4) column 4g + t%4, then lane (t/4 + 8) column 4g + t%4.
 __device__ __forceinline__ void st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
@@ -113,16 +130,26 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
+// Exact E4M3 -> fp16 for two bytes (hardware conversion): dec(b) itself;
+// |dec| <= 448 and the subnormal quantum 2^-9 are both exact in fp16.
+__device__ __forceinline__ uint32_t cvt2(uint32_t w16) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(w16));
+  return r;
+}
+__device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
+  return make_uint4(cvt2(a & 0xFFFFu), cvt2(a >> 16), cvt2(b & 0xFFFFu), cvt2(b >> 16));
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   using C = Cfg<D>;
-  constexpr int kChunks = D / 16;           // 16-byte raw chunks per token row
-  constexpr int kLoadsPerTile = kT * kChunks / 128;  // per loader thread, per K (and per V)
+  constexpr int kChunks = D / 16;                              // 16-byte raw chunks per token row
+  constexpr int kDecPerTile = kT * kChunks / kDecThreads;      // per decoder thread, per K (and per V)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + C::kOffQ;
   Meta& mt = *reinterpret_cast<Meta*>(smem + C::kOffMeta);
 
   const int tid = threadIdx.x;
@@ -168,30 +195,23 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   // ---------------------------------------------------------- setup
   if (tid == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&mt.kv_full[i], 128);
+      mbar_init(&mt.kv_full[i], kDecThreads);
       mbar_init(&mt.kv_empty[i], 1);
+    }
+    for (int i = 0; i < C::kRaw; ++i) {
+      mbar_init(&mt.raw_full[i], 1);
+      mbar_init(&mt.raw_empty[i], kDecThreads);
     }
     mbar_init(&mt.s_full[0], 1);
     mbar_init(&mt.s_full[1], 1);
-    mbar_init(&mt.p_ready, 128);
-    mbar_init(&mt.pv_done, 1);
+    mbar_init(&mt.pv_done[0], 1);
+    mbar_init(&mt.pv_done[1], 1);
+    mbar_init(&mt.p_ready, 32 * kSoftmaxWarps);
     mbar_init_fence();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&mt.tmem, C::kTmemCols);
     tmem_relinquish();
-  }
-  // Q rows -> swizzled K-major tile (rows >= RC are zero)
-  for (int idx = tid; idx < kRows * (D / 8); idx += kThreads) {
-    const int i = idx / (D / 8), c8 = idx % (D / 8);  // row, 8-element chunk
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (i < RC) {
-      const int rowi = row0 + i;
-      const int r = rowi / p.G, h = g * p.G + rowi % p.G;
-      v = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D + c8 * 8);
-    }
-    const int db = c8 / 8, ch = c8 % 8;
-    *reinterpret_cast<uint4*>(sQ + db * (kRows * 128) + i * 128 + ((ch ^ (i & 7)) * 16)) = v;
   }
   for (int i = tid; i < kRows; i += kThreads) {
     int n = -1;
@@ -201,128 +221,197 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     }
     mt.nrow[i] = n;
   }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = mt.tmem;
 
-  if (warp >= 4 && warp < 8) {
-    // ======================================================== loaders
-    const int lt = tid - 128;
-    uint4 kr[kLoadsPerTile], vr[kLoadsPerTile];
-    auto issue = [&](int i) {
+  if (warp < kSoftmaxWarps) {
+    // Q -> TMEM: lane 32w+j (j < 16) holds query vector 16w+j as fp16 pairs
+    // along the columns; lanes 32w+16..31 are zero rows.
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const int qi = 16 * warp + lane;
+    const bool has = (lane < 16) && (qi < RC);
+    const uint16_t* qp = nullptr;
+    if (has) {
+      const int rowi = row0 + qi;
+      const int r = rowi / p.G, h = g * p.G + rowi % p.G;
+      qp = p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D;
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < D / 2; c0 += 16) {
+      uint32_t v[16];
 #pragma unroll
-      for (int j = 0; j < kLoadsPerTile; ++j) {
-        const int L = j * 128 + lt;
-        const int t = L / kChunks, c = L % kChunks;
-        kr[j] = make_uint4(0, 0, 0, 0);
-        vr[j] = make_uint4(0, 0, 0, 0);
-        const uint8_t* kp = nullptr;
-        const uint8_t* vp = nullptr;
+      for (int j = 0; j < 16; j += 4) {
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (has) x = *reinterpret_cast<const uint4*>(qp + 2 * (c0 + j));
+        v[j] = x.x;
+        v[j + 1] = x.y;
+        v[j + 2] = x.z;
+        v[j + 3] = x.w;
+      }
+      tmem_st16(tmem + C::kColQ + lane_off + c0, v);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == kProdWarp) {
+    // ======================================================== producer
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int slot = i % C::kRaw;
+        if (i >= C::kRaw) {
+          if (!mbar_wait(&mt.raw_empty[slot], ((i / C::kRaw) - 1) & 1, kWaitLimit)) ok = false;
+        }
+        uint8_t* rK = smem + C::kOffRaw + slot * C::kRawBytes;
+        uint8_t* rV = rK + kT * D;
+        uint64_t* bar = &mt.raw_full[slot];
+        uint64_t valid = 0;
         if (MODE == FP8KV_MODE_DENSE) {
-          const int tok = u0 + i * kT + t;
-          if (tok < u1) {
-            const int blk = p.block_table[(int64_t)b * p.bt_stride + tok / p.page_size];
-            const int slot = tok % p.page_size;
-            if (blk >= 0 && blk < p.num_kv_blocks) {
-              kp = p.k_cache + blk * p.ksb + slot * p.kst + g * p.ksh;
-              vp = p.v_cache + blk * p.vsb + slot * p.vst + g * p.vsh;
-            } else if (c == 0) {
+          int t = 0;
+          while (t < kT) {
+            const int tok = u0 + i * kT + t;
+            if (tok >= u1) break;
+            const int page = tok / p.page_size, slot_in = tok % p.page_size;
+            const int blk = p.block_table[(int64_t)b * p.bt_stride + page];
+            const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
+            if (blk < 0 || blk >= p.num_kv_blocks) {
               set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
+              t += run;
+              continue;
             }
-          }
-        } else {
-          const int e = u0 + i * (kT / 4) + t / 4, tk = t % 4;
-          if (e < u1) {
-            const uint32_t mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
-            if ((mk & (0x11111111u << tk)) != 0u) {
-              const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-              if (blk >= 0 && blk < p.num_kv_blocks) {
-                kp = p.k_cache + blk * p.ksb + tk * p.kst + g * p.ksh;
-                vp = p.v_cache + blk * p.vsb + tk * p.vst + g * p.vsh;
-              } else if (c == 0 && tk == 0) {
-                set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
+            const uint8_t* ks = p.k_cache + blk * p.ksb + slot_in * p.kst + g * p.ksh;
+            const uint8_t* vs = p.v_cache + blk * p.vsb + slot_in * p.vst + g * p.vsh;
+            // rows of consecutive slots are adjacent when the token stride is D
+            if (p.kst == D) {
+              mbar_expect_tx(bar, run * D);
+              bulk_g2s(rK + t * D, ks, run * D, bar);
+            } else {
+              for (int r = 0; r < run; ++r) {
+                mbar_expect_tx(bar, D);
+                bulk_g2s(rK + (t + r) * D, ks + r * p.kst, D, bar);
               }
             }
+            if (p.vst == D) {
+              mbar_expect_tx(bar, run * D);
+              bulk_g2s(rV + t * D, vs, run * D, bar);
+            } else {
+              for (int r = 0; r < run; ++r) {
+                mbar_expect_tx(bar, D);
+                bulk_g2s(rV + (t + r) * D, vs + r * p.vst, D, bar);
+              }
+            }
+            valid |= ((run == 64) ? ~0ull : ((1ull << run) - 1ull)) << t;
+            t += run;
+          }
+        } else {
+          for (int el = 0; el < kT / 4; ++el) {
+            const int e = u0 + i * (kT / 4) + el;
+            uint32_t mk = 0;
+            if (e < u1) {
+              mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
+              const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
+              if (mk != 0u && (blk < 0 || blk >= p.num_kv_blocks)) {
+                set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
+                mk = 0;
+              }
+              if (mk != 0u) {
+                // only tokens that at least one query row attends are copied
+                for (int tk = 0; tk < 4; ++tk) {
+                  if ((mk & (0x11111111u << tk)) == 0u) continue;
+                  const int t = el * 4 + tk;
+                  mbar_expect_tx(bar, 2 * D);
+                  bulk_g2s(rK + t * D, p.k_cache + blk * p.ksb + tk * p.kst + g * p.ksh, D, bar);
+                  bulk_g2s(rV + t * D, p.v_cache + blk * p.vsb + tk * p.vst + g * p.vsh, D, bar);
+                  valid |= 1ull << t;
+                }
+              }
+            }
+            mt.raw_masks[slot][el] = mk;
           }
         }
-        if (kp) {
-          kr[j] = __ldg(reinterpret_cast<const uint4*>(kp) + c);
-          vr[j] = __ldg(reinterpret_cast<const uint4*>(vp) + c);
-        }
+        mt.valid[slot] = valid;
+        mbar_arrive(bar);
       }
-    };
-    issue(0);
+      if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
+    // ======================================================== decoders
+    const int lt = tid - 32 * kSoftmaxWarps;
+    bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
+      const int slot = i % C::kRaw;
       const int st = i % C::kStages;
+      if (!mbar_wait(&mt.raw_full[slot], (i / C::kRaw) & 1, kWaitLimit)) ok = false;
       if (i >= C::kStages) {
-        if (!mbar_wait(&mt.kv_empty[st], ((i / C::kStages) - 1) & 1, kWaitLimit))
-          set_status(p.status, FP8KV_STATUS_TIMEOUT);
+        if (!mbar_wait(&mt.kv_empty[st], ((i / C::kStages) - 1) & 1, kWaitLimit)) ok = false;
       }
+      const uint8_t* rK = smem + C::kOffRaw + slot * C::kRawBytes;
+      const uint8_t* rV = rK + kT * D;
       uint8_t* sK = smem + C::kOffStages + st * C::kStageBytes;
       uint8_t* sV = sK + C::kKVBytes;
-      if (MODE == FP8KV_MODE_SPARSE_PAGE4 && lt < 16) {
-        const int e = u0 + i * (kT / 4) + lt;
-        uint32_t mk = 0;
-        if (e < u1) {
-          mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
-          const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-          if (blk < 0 || blk >= p.num_kv_blocks) mk = 0;
-        }
-        mt.masks[st][lt] = mk;
+      const uint64_t valid = mt.valid[slot];
+      if (MODE == FP8KV_MODE_SPARSE_PAGE4 && lt < 16) mt.masks[st][lt] = mt.raw_masks[slot][lt];
+      uint4 kw[kDecPerTile], vw[kDecPerTile];
+#pragma unroll
+      for (int j = 0; j < kDecPerTile; ++j) {
+        const int L = j * kDecThreads + lt;
+        const int t = L / kChunks, c = L % kChunks;
+        const bool ok_t = (valid >> t) & 1ull;
+        kw[j] = ok_t ? *reinterpret_cast<const uint4*>(rK + t * D + c * 16) : make_uint4(0, 0, 0, 0);
+        vw[j] = ok_t ? *reinterpret_cast<const uint4*>(rV + t * D + c * 16) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int j = 0; j < kLoadsPerTile; ++j) {
-        const int L = j * 128 + lt;
+      for (int j = 0; j < kDecPerTile; ++j) {
+        const int L = j * kDecThreads + lt;
         const int t = L / kChunks, c = L % kChunks;
         const int db = c / 4;
         const int h0 = (c % 4) * 2;  // first of the two 16-byte fp16 chunks
         // alternate the order of the two stores between column blocks so the
         // eight threads of a store phase hit eight different bank groups
-        const int first = (db & 1) ? h0 + 1 : h0;
-        const int second = (db & 1) ? h0 : h0 + 1;
+        const bool swap = (db & 1) != 0;
+        const int first = swap ? h0 + 1 : h0;
+        const int second = swap ? h0 : h0 + 1;
         uint8_t* rowK = sK + db * (kT * 128) + t * 128;
         uint8_t* rowV = sV + db * (kT * 128) + t * 128;
-        const uint32_t kw[4] = {kr[j].x, kr[j].y, kr[j].z, kr[j].w};
-        const uint32_t vw[4] = {vr[j].x, vr[j].y, vr[j].z, vr[j].w};
-        uint4 k0, k1, v0, v1;
-        k0 = make_uint4(e4m3x2_to_f16x2_lo(kw[0]), e4m3x2_to_f16x2_hi(kw[0]), e4m3x2_to_f16x2_lo(kw[1]),
-                        e4m3x2_to_f16x2_hi(kw[1]));
-        k1 = make_uint4(e4m3x2_to_f16x2_lo(kw[2]), e4m3x2_to_f16x2_hi(kw[2]), e4m3x2_to_f16x2_lo(kw[3]),
-                        e4m3x2_to_f16x2_hi(kw[3]));
-        v0 = make_uint4(e4m3x2_to_f16x2_lo(vw[0]), e4m3x2_to_f16x2_hi(vw[0]), e4m3x2_to_f16x2_lo(vw[1]),
-                        e4m3x2_to_f16x2_hi(vw[1]));
-        v1 = make_uint4(e4m3x2_to_f16x2_lo(vw[2]), e4m3x2_to_f16x2_hi(vw[2]), e4m3x2_to_f16x2_lo(vw[3]),
-                        e4m3x2_to_f16x2_hi(vw[3]));
+        const uint4 k0 = dec8(kw[j].x, kw[j].y), k1 = dec8(kw[j].z, kw[j].w);
+        const uint4 v0 = dec8(vw[j].x, vw[j].y), v1 = dec8(vw[j].z, vw[j].w);
         const int sw = t & 7;
-        *reinterpret_cast<uint4*>(rowK + ((first ^ sw) * 16)) = (first == h0) ? k0 : k1;
-        *reinterpret_cast<uint4*>(rowK + ((second ^ sw) * 16)) = (first == h0) ? k1 : k0;
-        *reinterpret_cast<uint4*>(rowV + ((first ^ sw) * 16)) = (first == h0) ? v0 : v1;
-        *reinterpret_cast<uint4*>(rowV + ((second ^ sw) * 16)) = (first == h0) ? v1 : v0;
+        *reinterpret_cast<uint4*>(rowK + ((first ^ sw) * 16)) = swap ? k1 : k0;
+        *reinterpret_cast<uint4*>(rowK + ((second ^ sw) * 16)) = swap ? k0 : k1;
+        *reinterpret_cast<uint4*>(rowV + ((first ^ sw) * 16)) = swap ? v1 : v0;
+        *reinterpret_cast<uint4*>(rowV + ((second ^ sw) * 16)) = swap ? v0 : v1;
       }
       fence_proxy_async_smem();
       mbar_arrive(&mt.kv_full[st]);
-      if (i + 1 < n_tiles) issue(i + 1);
+      mbar_arrive(&mt.raw_empty[slot]);
     }
-  } else if (warp == 8) {
+    if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
+  } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16_f32(64, kT, false, false);
+      const uint32_t idesc_qk = idesc_f16_f32(128, kT, false, false);
       const uint32_t idesc_pv = idesc_f16_f32(128, D, false, true);
-      const uint32_t sq = smem_u32(sQ);
       bool ok = true;
       for (int i = 0; i <= n_tiles; ++i) {
         if (i < n_tiles) {
           const int st = i % C::kStages;
           if (!mbar_wait(&mt.kv_full[st], (i / C::kStages) & 1, kWaitLimit)) ok = false;
+          // S(i) overwrites the buffer that held P(i-2): PV(i-2) must be done
+          if (i >= 2) {
+            if (!mbar_wait(&mt.pv_done[i & 1], ((i - 2) >> 1) & 1, kWaitLimit)) ok = false;
+          }
           tc_fence_after();
           const uint32_t sk = smem_u32(smem + C::kOffStages + st * C::kStageBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = smem_desc(sq + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSw128);
             const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-            mma_ss(tmem + C::kColS + (i & 1) * kT, ad, bd, idesc_qk, kk > 0);
+            mma_ts(tmem + C::kColS + (i & 1) * kT, tmem + C::kColQ + kk * 8, bd, idesc_qk, kk > 0);
           }
           mma_commit(&mt.s_full[i & 1]);
         }
@@ -335,10 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
             const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
-            mma_ts(tmem + C::kColO, tmem + C::kColP + (j & 1) * (kT / 2) + kk * 8, bd, idesc_pv,
+            mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * kT + kk * 8, bd, idesc_pv,
                    (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&mt.pv_done);
+          mma_commit(&mt.pv_done[j & 1]);
           mma_commit(&mt.kv_empty[st]);
         }
       }
@@ -348,133 +437,145 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   } else {
     // ======================================================== softmax warps
     const float ks = p.k_scale_dev ? *p.k_scale_dev : p.k_scale;
-    // base-2 logit factor; K was decoded as value * 2^-8
-    const float c = p.softmax_scale * ks * kLog2e * 256.0f;
+    // base-2 logit factor (K is decoded to its exact value)
+    const float c = p.softmax_scale * ks * kLog2e;
     const int ra = 16 * warp + (lane >> 2);  // this thread's two rows: ra and ra + 8
     const int rb = ra + 8;
     const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const bool warp_live = 16 * warp < RC;   // warps without query vectors only keep the barriers
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     const int n_a = mt.nrow[ra], n_b = mt.nrow[rb];
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       if (!mbar_wait(&mt.s_full[i & 1], (i >> 1) & 1, kWaitLimit)) ok = false;
       tc_fence_after();
-      uint32_t sr[32];
-      ld_16x256b_x8(tmem + C::kColS + (i & 1) * kT + lane_off, sr);
-      tmem_ld_wait();
-      // visibility of this thread's 16 columns for rows ra, rb
-      float sa[16], sb[16];
-      uint32_t vis = 0;  // bit e: row ra column e, bit 16 + e: row rb column e
       const int st = i % C::kStages;
       if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
-        // the tile's masks were published by the loaders with kv_full[st]
+        // the tile's masks were published by the decoders with kv_full[st]
         if (!mbar_wait(&mt.kv_full[st], (i / C::kStages) & 1, kWaitLimit)) ok = false;
       }
-      float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-      for (int gq = 0; gq < 8; ++gq) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = 8 * gq + 2 * (lane & 3) + e;
-          bool va, vb;
-          if (MODE == FP8KV_MODE_DENSE) {
-            const int tok = u0 + i * kT + col;
-            va = (tok < u1) && (tok < n_a);
-            vb = (tok < u1) && (tok < n_b);
+      if (warp_live) {
+        uint32_t sr[32];
+        ld_16x256b_x8(tmem + C::kColS + (i & 1) * kT + lane_off, sr);
+        tmem_ld_wait();
+        // visibility of this thread's 16 columns for rows ra (bits 0..15) and rb (16..31)
+        uint32_t vis;
+        if (MODE == FP8KV_MODE_DENSE) {
+          const int t0 = u0 + i * kT;
+          const int lim_a = min(u1, n_a) - t0, lim_b = min(u1, n_b) - t0;
+          if (lim_a >= kT && lim_b >= kT) {
+            vis = 0xFFFFFFFFu;
           } else {
-            const int ent = u0 + i * (kT / 4) + col / 4;
-            const uint32_t mk = (ent < u1) ? mt.masks[st][col / 4] : 0u;
-            va = (n_a >= 0) && ((mk >> (4 * n_a + (col & 3))) & 1u);
-            vb = (n_b >= 0) && ((mk >> (4 * n_b + (col & 3))) & 1u);
+            vis = 0;
+#pragma unroll
+            for (int gq = 0; gq < 8; ++gq)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int col = 8 * gq + 2 * (lane & 3) + e;
+                vis |= (col < lim_a ? 1u : 0u) << (2 * gq + e);
+                vis |= (col < lim_b ? 1u : 0u) << (16 + 2 * gq + e);
+              }
           }
-          const float xa = __uint_as_float(sr[4 * gq + e]);
-          const float xb = __uint_as_float(sr[4 * gq + 2 + e]);
-          sa[2 * gq + e] = xa;
-          sb[2 * gq + e] = xb;
-          vis |= (va ? 1u : 0u) << (2 * gq + e);
-          vis |= (vb ? 1u : 0u) << (16 + 2 * gq + e);
-          if (va) mx_a = fmaxf(mx_a, xa * c);
-          if (vb) mx_b = fmaxf(mx_b, xb * c);
-        }
-      }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      // lazy integer max
-      const float mn_a = (mx_a > m_a + kTau || m_a == -INFINITY) ? fmaxf(m_a, ceilf(mx_a)) : m_a;
-      const float mn_b = (mx_b > m_b + kTau || m_b == -INFINITY) ? fmaxf(m_b, ceilf(mx_b)) : m_b;
-      const bool resc_a = (i > 0) && (m_a != -INFINITY) && (mn_a != m_a);
-      const bool resc_b = (i > 0) && (m_b != -INFINITY) && (mn_b != m_b);
-      const float alpha_a = resc_a ? exp2_int(m_a - mn_a) : 1.f;
-      const float alpha_b = resc_b ? exp2_int(m_b - mn_b) : 1.f;
-      m_a = mn_a;
-      m_b = mn_b;
-      const float mu_a = (m_a == -INFINITY) ? 0.f : m_a;
-      const float mu_b = (m_b == -INFINITY) ? 0.f : m_b;
-      uint32_t ph[16], pl[16];
-      float sum_a = 0.f, sum_b = 0.f;
+        } else {
+          vis = 0;
 #pragma unroll
-      for (int q2 = 0; q2 < 8; ++q2) {
-        // masked tokens get exactly 0 by selection (never 0 * x arithmetic)
-        const float pa0 = ((vis >> (2 * q2)) & 1u) ? exp2f(fmaf(sa[2 * q2], c, -mu_a)) : 0.f;
-        const float pa1 = ((vis >> (2 * q2 + 1)) & 1u) ? exp2f(fmaf(sa[2 * q2 + 1], c, -mu_a)) : 0.f;
-        const float pb0 = ((vis >> (16 + 2 * q2)) & 1u) ? exp2f(fmaf(sb[2 * q2], c, -mu_b)) : 0.f;
-        const float pb1 = ((vis >> (16 + 2 * q2 + 1)) & 1u) ? exp2f(fmaf(sb[2 * q2 + 1], c, -mu_b)) : 0.f;
-        sum_a += pa0 + pa1;
-        sum_b += pb0 + pb1;
-        const uint32_t ha = pack_f16x2(pa0, pa1), hb = pack_f16x2(pb0, pb1);
-        const float2 fa = unpack_f16x2(ha), fb = unpack_f16x2(hb);
-        ph[2 * q2] = ha;
-        ph[2 * q2 + 1] = hb;
-        pl[2 * q2] = pack_f16x2(pa0 - fa.x, pa1 - fa.y);
-        pl[2 * q2 + 1] = pack_f16x2(pb0 - fb.x, pb1 - fb.y);
-      }
-      sum_a += __shfl_xor_sync(0xffffffffu, sum_a, 1);
-      sum_a += __shfl_xor_sync(0xffffffffu, sum_a, 2);
-      sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 1);
-      sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 2);
-      l_a = l_a * alpha_a + sum_a;
-      l_b = l_b * alpha_b + sum_b;
+          for (int gq = 0; gq < 8; ++gq)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = 8 * gq + 2 * (lane & 3) + e;
+              const int ent = u0 + i * (kT / 4) + col / 4;
+              const uint32_t mk = (ent < u1) ? mt.masks[st][col / 4] : 0u;
+              vis |= ((n_a >= 0) ? ((mk >> (4 * n_a + (col & 3))) & 1u) : 0u) << (2 * gq + e);
+              vis |= ((n_b >= 0) ? ((mk >> (4 * n_b + (col & 3))) & 1u) : 0u) << (16 + 2 * gq + e);
+            }
+        }
+        float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+        for (int gq = 0; gq < 8; ++gq)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if ((vis >> (2 * gq + e)) & 1u) mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * gq + e]) * c);
+            if ((vis >> (16 + 2 * gq + e)) & 1u) mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * gq + 2 + e]) * c);
+          }
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+        // lazy integer max
+        const float mn_a = (mx_a > m_a + kTau || m_a == -INFINITY) ? fmaxf(m_a, ceilf(mx_a)) : m_a;
+        const float mn_b = (mx_b > m_b + kTau || m_b == -INFINITY) ? fmaxf(m_b, ceilf(mx_b)) : m_b;
+        const bool resc_a = (i > 0) && (m_a != -INFINITY) && (mn_a != m_a);
+        const bool resc_b = (i > 0) && (m_b != -INFINITY) && (mn_b != m_b);
+        const float alpha_a = resc_a ? exp2_int(m_a - mn_a) : 1.f;
+        const float alpha_b = resc_b ? exp2_int(m_b - mn_b) : 1.f;
+        m_a = mn_a;
+        m_b = mn_b;
+        const float mu_a = (m_a == -INFINITY) ? 0.f : m_a;
+        const float mu_b = (m_b == -INFINITY) ? 0.f : m_b;
+        uint32_t ph[16], pl[16];
+        float sum_a = 0.f, sum_b = 0.f;
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) {
+          // masked tokens get exactly 0 by selection (never 0 * x arithmetic)
+          const float pa0 =
+              ((vis >> (2 * q2)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2]), c, -mu_a)) : 0.f;
+          const float pa1 =
+              ((vis >> (2 * q2 + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 1]), c, -mu_a)) : 0.f;
+          const float pb0 =
+              ((vis >> (16 + 2 * q2)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 2]), c, -mu_b)) : 0.f;
+          const float pb1 =
+              ((vis >> (17 + 2 * q2)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 3]), c, -mu_b)) : 0.f;
+          sum_a += pa0 + pa1;
+          sum_b += pb0 + pb1;
+          const uint32_t ha = pack_f16x2(pa0, pa1), hb = pack_f16x2(pb0, pb1);
+          const float2 fa = unpack_f16x2(ha), fb = unpack_f16x2(hb);
+          ph[2 * q2] = ha;
+          ph[2 * q2 + 1] = hb;
+          pl[2 * q2] = pack_f16x2(pa0 - fa.x, pa1 - fa.y);
+          pl[2 * q2 + 1] = pack_f16x2(pb0 - fb.x, pb1 - fb.y);
+        }
+        sum_a += __shfl_xor_sync(0xffffffffu, sum_a, 1);
+        sum_a += __shfl_xor_sync(0xffffffffu, sum_a, 2);
+        sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 1);
+        sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 2);
+        l_a = l_a * alpha_a + sum_a;
+        l_b = l_b * alpha_b + sum_b;
 
-      // PV(i-1) must be complete before P's buffer (i&1, last read by PV(i-2))
-      // is rewritten and before O can be rescaled.
-      if (i >= 1) {
-        if (!mbar_wait(&mt.pv_done, (i - 1) & 1, kWaitLimit)) ok = false;
-        tc_fence_after();
-      }
-      const bool any_resc = __any_sync(0xffffffffu, resc_a || resc_b);
-      if (any_resc) {
-        // O rows of this warp: lanes 32w + (0..15) hold P_hi rows, +16 the P_lo
-        // twins; thread `lane` owns TMEM lane 32w + lane = row 16w + lane%16.
-        const int myrow_local = lane & 15;  // row 16w + myrow_local
-        // alpha of row 16w + x lives in thread 4*(x%8) (+ for rows x >= 8: b)
-        const float al_src_a = __shfl_sync(0xffffffffu, alpha_a, 4 * (myrow_local & 7));
-        const float al_src_b = __shfl_sync(0xffffffffu, alpha_b, 4 * (myrow_local & 7));
-        const float al = (myrow_local < 8) ? al_src_a : al_src_b;
+        if (__any_sync(0xffffffffu, resc_a || resc_b)) {
+          // O must hold every earlier tile before it is rescaled: wait PV(i-1)
+          if (!mbar_wait(&mt.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimit)) ok = false;
+          tc_fence_after();
+          // thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16 (the
+          // P_hi row for lane < 16, its P_lo twin above); the alpha of vector
+          // 16w + x lives in thread 4*(x%8), as its a (x < 8) or b value.
+          const int x = lane & 15;
+          const float al_a = __shfl_sync(0xffffffffu, alpha_a, 4 * (x & 7));
+          const float al_b = __shfl_sync(0xffffffffu, alpha_b, 4 * (x & 7));
+          const float al = (x < 8) ? al_a : al_b;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld16(tmem + C::kColO + lane_off + c0, o);
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tmem + C::kColO + lane_off + c0, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
-          tmem_st16(tmem + C::kColO + lane_off + c0, o);
+            for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
+            tmem_st16(tmem + C::kColO + lane_off + c0, o);
+          }
         }
+        // P(i) replaces S(i) in its buffer: hi in lanes 32w+0..15, lo 16 above
+        const uint32_t pcol = tmem + C::kColS + (i & 1) * kT + lane_off;
+        st_16x128b_x8(pcol, ph);
+        st_16x128b_x8(pcol + (16u << 16), pl);
         tmem_st_wait();
       }
-      const uint32_t pcol = tmem + C::kColP + (i & 1) * (kT / 2) + lane_off;
-      st_16x128b_x8(pcol, ph);
-      st_16x128b_x8(pcol + (16u << 16), pl);
-      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&mt.p_ready);
     }
     // ------------------------------------------------------ epilogue
-    if (!mbar_wait(&mt.pv_done, (n_tiles - 1) & 1, kWaitLimit)) ok = false;
+    if (!mbar_wait(&mt.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, kWaitLimit)) ok = false;
     tc_fence_after();
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
-    {
+    if (warp_live) {
       const int myrow = 16 * warp + (lane & 15);
       float* dst = p.partial + (prow + myrow) * D;
 #pragma unroll 1
@@ -485,14 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float x = __uint_as_float(o[j]);
-          v[j] = x + __shfl_down_sync(0xffffffffu, x, 16);
+          const float xo = __uint_as_float(o[j]);
+          v[j] = xo + __shfl_down_sync(0xffffffffu, xo, 16);
         }
         if (lane < 16 && myrow < RC) {
 #pragma unroll
           for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4*>(dst + c0 + j) =
-                make_float4(v[j] * 256.f, v[j + 1] * 256.f, v[j + 2] * 256.f, v[j + 3] * 256.f);
+            *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
       }
       if ((lane & 3) == 0) {
@@ -504,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
