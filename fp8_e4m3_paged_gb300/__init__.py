@@ -9,7 +9,7 @@ ImportError.
 
 _EXPORTS = (
     "Args", "Call", "Desc", "Fp8kvError", "Plan",
-    "fp8kv_attn_combine", "fp8kv_attn_plan", "fp8kv_attn_split",
+    "fp8kv_attn_combine", "fp8kv_attn_forward_static", "fp8kv_attn_plan", "fp8kv_attn_split",
     "fp8kv_attn_strerror", "fp8kv_attn_version", "make_args", "make_desc",
 )
 

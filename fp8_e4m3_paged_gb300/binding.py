@@ -87,7 +87,9 @@ lib.fp8kv_attn_strerror.restype = ctypes.c_char_p
 lib.fp8kv_attn_strerror.argtypes = [ctypes.c_int]
 lib.fp8kv_attn_plan.restype = ctypes.c_int
 lib.fp8kv_attn_plan.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Plan)]
-for _n in ("fp8kv_attn_split", "fp8kv_attn_combine"):
+STATIC_SCRATCH_BYTES = 16 << 20
+
+for _n in ("fp8kv_attn_split", "fp8kv_attn_combine", "fp8kv_attn_forward_static"):
     getattr(lib, _n).restype = ctypes.c_int
     getattr(lib, _n).argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), ctypes.c_void_p]
 
@@ -124,6 +126,13 @@ def fp8kv_attn_combine(plan: Plan, args: Args, stream: int = 0) -> None:
     rc = lib.fp8kv_attn_combine(ctypes.byref(plan), ctypes.byref(args), ctypes.c_void_p(stream))
     if rc != OK:
         raise Fp8kvError(rc, "fp8kv_attn_combine")
+
+
+def fp8kv_attn_forward_static(plan: Plan, args: Args, stream: int = 0) -> None:
+    """Split + combine using the library's own device scratch (no workspace)."""
+    rc = lib.fp8kv_attn_forward_static(ctypes.byref(plan), ctypes.byref(args), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_forward_static")
 
 
 # ---------------------------------------------------------------- torch glue

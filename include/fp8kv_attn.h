@@ -185,6 +185,28 @@ int fp8kv_attn_split(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
 int fp8kv_attn_combine(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
                        fp8kv_stream_t stream);
 
+/* Size of the library-owned device scratch used by fp8kv_attn_forward_static
+ * (16 MiB; one copy per GPU that loads the library, held until exit). */
+#define FP8KV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* Split + combine without a caller-provided workspace, for callers that cannot
+ * allocate device memory (a host runtime that hands a plugin only its input
+ * and output buffers, a memory manager that owns the whole device heap, or a
+ * path that forbids allocator calls).  This entry point has no counterpart in
+ * the pages; it exists for those callers.
+ *
+ * The FP32 partials and the status word live in a file-scope device array of
+ * FP8KV_STATIC_SCRATCH_BYTES; plans needing more return FP8KV_EWORKSPACE.
+ * Nothing is allocated or freed.  `a` is used as for fp8kv_attn_split except
+ * that a->workspace is not the scratch: if it is non-NULL and
+ * a->workspace_bytes >= 4, the call's 32-bit status word is copied there (in
+ * stream order) after the combine.  The first call on a device looks the
+ * array's address up for that device; make it before any stream capture.
+ * Every call shares the one array: calls whose kernels may overlap on the GPU
+ * (other streams, other host threads) race on it and must be serialised. */
+int fp8kv_attn_forward_static(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
+                              fp8kv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
