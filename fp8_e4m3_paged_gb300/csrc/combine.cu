@@ -5,15 +5,18 @@
 //
 // written as fp16 with round-to-nearest-even.  A query vector whose total L is
 // 0 (dead row, or nothing visible) gets +0.0.  Partitions with l_s = 0 are
-// skipped by a branch, so their numerators are never read.  The partition
+// skipped by selection, so their numerators are never read.  The partition
 // maxima are integers (base-2 units), so every w_s is an exact power of two
 // ("DFlash2 E4M3 attention with FP32 state", intro paragraph 4: FP32
 // combination, FP16 final activation; "Qwen4Exp: fp8_e4m3 main KV cache on
 // the QSA path", review: v_scale acts as the output scale).
 //
 // One CTA per (query vector, 64-wide slice of D); its 256 threads are 16
-// partition lanes x 16 float4 columns, so the partitions of one vector are
-// read in parallel and reduced in shared memory in a fixed order.
+// partition lanes x 16 float4 columns.  The kernel is latency-bound (a few
+// MB in total), so it makes two dependent trips to memory: the (m, l) pairs
+// of all partitions (held in registers for the weights), then every
+// numerator a lane needs, all loads issued before the first FMA.  The lanes
+// are reduced in shared memory in a fixed order.
 #include <cstdint>
 
 #include <cuda_fp16.h>
@@ -26,9 +29,11 @@ namespace fp8kv {
 namespace {
 
 constexpr int CT = 256;
-constexpr int SL = 16;    // partition lanes
-constexpr int DW = 64;    // d slice per CTA
-constexpr int MAXS = 1024;  // partitions staged in shared memory per pass
+constexpr int SL = 16;      // partition lanes
+constexpr int DW = 64;      // d slice per CTA
+constexpr int MAXS = 1024;  // partitions whose weights are staged per pass
+constexpr int KR = MAXS / CT;  // (m, l) pairs a thread holds
+constexpr int NB = 8;       // numerator loads in flight per lane
 
 __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   __shared__ float red_m[CT / 32];
@@ -49,10 +54,24 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   const float2* ml = p.ml + base;           // partition s at ml[s * rows]
   const int64_t sstride = p.rows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = p.S;
 
-  // global max over live partitions (all (m, l) pairs read in parallel)
+  // global max over live partitions; the first MAXS pairs stay in registers
+  float mv[KR], lv[KR];
   float M = -INFINITY;
-  for (int s = tid; s < p.S; s += CT) {
+#pragma unroll
+  for (int k = 0; k < KR; ++k) {
+    const int s = tid + k * CT;
+    mv[k] = -INFINITY;
+    lv[k] = 0.f;
+    if (s < S) {
+      const float2 v = ml[s * sstride];
+      mv[k] = v.x;
+      lv[k] = v.y;
+      if (v.y > 0.f) M = fmaxf(M, v.x);
+    }
+  }
+  for (int s = tid + MAXS; s < S; s += CT) {
     const float2 v = ml[s * sstride];
     if (v.y > 0.f) M = fmaxf(M, v.x);
   }
@@ -68,26 +87,49 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
   const float* acc = p.partial + base * D + slice * DW + c4 * 4;
-  for (int s0 = 0; s0 < p.S && M != -INFINITY; s0 += MAXS) {
-    const int ns = min(MAXS, p.S - s0);
-    __syncthreads();
-    for (int k = tid; k < ns; k += CT) {
-      const float2 v = ml[(s0 + k) * sstride];
-      const bool live = v.y > 0.f;
-      s_w[k] = live ? exp2_int(v.x - M) : 0.f;  // integer maxima: exact
-      s_l[k] = live ? v.y : 0.f;
+  for (int s0 = 0; s0 < S && M != -INFINITY; s0 += MAXS) {
+    const int ns = min(MAXS, S - s0);
+    if (s0 > 0) __syncthreads();
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int kk = tid + k * CT;
+      if (kk < ns) {
+        float m_s, l_s;
+        if (s0 == 0) {
+          m_s = mv[k];
+          l_s = lv[k];
+        } else {
+          const float2 v = ml[(s0 + kk) * sstride];
+          m_s = v.x;
+          l_s = v.y;
+        }
+        const bool live = l_s > 0.f;
+        s_w[kk] = live ? exp2_int(m_s - M) : 0.f;  // integer maxima: exact
+        s_l[kk] = live ? l_s : 0.f;
+      }
     }
     __syncthreads();
-#pragma unroll 4
-    for (int k = sl; k < ns; k += SL) {
-      const float w = s_w[k];
-      if (w != 0.f) {  // dead partitions' numerators are never read
-        const float4 a = *reinterpret_cast<const float4*>(acc + (int64_t)(s0 + k) * sstride * D);
-        o.x = fmaf(w, a.x, o.x);
-        o.y = fmaf(w, a.y, o.y);
-        o.z = fmaf(w, a.z, o.z);
-        o.w = fmaf(w, a.w, o.w);
-        L = fmaf(w, s_l[k], L);
+    for (int k0 = sl; k0 < ns; k0 += SL * NB) {
+      float4 a[NB];
+      float w[NB];
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const int k = k0 + j * SL;
+        w[j] = (k < ns) ? s_w[k] : 0.f;
+        // dead partitions' numerators are never read
+        a[j] = (w[j] != 0.f) ? *reinterpret_cast<const float4*>(acc + (int64_t)(s0 + k) * sstride * D)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const int k = k0 + j * SL;
+        if (w[j] != 0.f) {
+          o.x = fmaf(w[j], a[j].x, o.x);
+          o.y = fmaf(w[j], a[j].y, o.y);
+          o.z = fmaf(w[j], a[j].z, o.z);
+          o.w = fmaf(w[j], a[j].w, o.w);
+          L = fmaf(w[j], s_l[k], L);
+        }
       }
     }
   }
@@ -127,8 +169,8 @@ cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaS
   const int64_t n = (int64_t)p.B * p.q_max * p.Hq * (p.D / DW);
   if (n == 0) return cudaSuccess;
   if (p.D % DW) return cudaErrorInvalidValue;
-  combine_kernel<<<(unsigned)n, CT, 0, st>>>(p);
   (void)plan;
+  combine_kernel<<<(unsigned)n, CT, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ constexpr int kProdWarp = kMmaWarp + 1;               // 13
 constexpr int kThreads = 32 * (kProdWarp + 1);        // 448
 constexpr float kTau = 8.0f;        // lazy-rescale threshold (base-2 units)
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kSpinLimit = 1u << 24;  // consecutive idle probes of the MMA issuer
 constexpr int kMaxStages = 4;
 
 template <int D>
@@ -398,37 +399,48 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       const uint32_t idesc_qk = idesc_f16_f32(128, kT, false, false);
       const uint32_t idesc_pv = idesc_f16_f32(128, D, false, true);
       bool ok = true;
-      for (int i = 0; i <= n_tiles; ++i) {
-        if (i < n_tiles) {
-          const int st = i % C::kStages;
-          if (!mbar_wait(&mt.kv_full[st], (i / C::kStages) & 1, kWaitLimit)) ok = false;
-          // S(i) overwrites the buffer that held P(i-2): PV(i-2) must be done
-          if (i >= 2) {
-            if (!mbar_wait(&mt.pv_done[i & 1], ((i - 2) >> 1) & 1, kWaitLimit)) ok = false;
-          }
-          tc_fence_after();
-          const uint32_t sk = smem_u32(smem + C::kOffStages + st * C::kStageBytes);
+      // Step i holds two independent chains: the QK of tile i and the PV of
+      // tile i-1.  Whichever is ready first is issued first, so a PV never
+      // waits behind the decode of the next tile (the decoders in turn wait
+      // for that PV to free an operand stage).  Readiness is probed between
+      // whole chains only: an mbarrier probe right after a UMMA stalls the
+      // issuing thread for about the UMMA's latency.
+      uint32_t spins = 0;
+      for (int i = 0; i <= n_tiles && ok; ++i) {
+        const int j = i - 1;
+        bool qk_todo = i < n_tiles, pv_todo = i >= 1;
+        while (qk_todo || pv_todo) {
+          if (pv_todo && mbar_test(&mt.p_ready, j & 1)) {
+            tc_fence_after();
+            const int st = j % C::kStages;
+            const uint32_t sv = smem_u32(smem + C::kOffStages + st * C::kStageBytes + C::kKVBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-            mma_ts(tmem + C::kColS + (i & 1) * kT, tmem + C::kColQ + kk * 8, bd, idesc_qk, kk > 0);
-          }
-          mma_commit(&mt.s_full[i & 1]);
-        }
-        if (i >= 1) {
-          const int j = i - 1;
-          const int st = j % C::kStages;
-          if (!mbar_wait(&mt.p_ready, j & 1, kWaitLimit)) ok = false;
-          tc_fence_after();
-          const uint32_t sv = smem_u32(smem + C::kOffStages + st * C::kStageBytes + C::kKVBytes);
+            for (int kk = 0; kk < kT / 16; ++kk) {
+              const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
+              mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * kT + kk * 8, bd, idesc_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&mt.pv_done[j & 1]);
+            mma_commit(&mt.kv_empty[st]);
+            pv_todo = false;
+            spins = 0;
+          } else if (qk_todo && mbar_test(&mt.kv_full[i % C::kStages], (i / C::kStages) & 1) &&
+                     // S(i) overwrites the buffer that held P(i-2): PV(i-2) must be done
+                     (i < 2 || mbar_test(&mt.pv_done[i & 1], ((i - 2) >> 1) & 1))) {
+            tc_fence_after();
+            const uint32_t sk = smem_u32(smem + C::kOffStages + (i % C::kStages) * C::kStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk) {
-            const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
-            mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * kT + kk * 8, bd, idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
+              mma_ts(tmem + C::kColS + (i & 1) * kT, tmem + C::kColQ + kk * 8, bd, idesc_qk, kk > 0);
+            }
+            mma_commit(&mt.s_full[i & 1]);
+            qk_todo = false;
+            spins = 0;
+          } else if (++spins > kSpinLimit) {
+            ok = false;
+            break;
           }
-          mma_commit(&mt.pv_done[j & 1]);
-          mma_commit(&mt.kv_empty[st]);
         }
       }
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
