@@ -3,14 +3,20 @@
 //
 // Per CTA: one partition (a contiguous token range, or entry range in the
 // sparse microblock mode) of one (request, KV head, row chunk).  Warp roles:
-//   warp 13      producer (one thread): bulk copies (cp.async.bulk) of the
-//                tile's E4M3 K/V rows from the paged cache into a ring of raw
-//                shared-memory stages, completion counted in bytes on an
-//                mbarrier; runs of tokens contiguous in a page move as one
-//                copy; tokens no query row may see are never copied;
-//   warps 4-11   decoders: raw E4M3 -> exact fp16 with the hardware
-//                e4m3x2 -> f16x2 conversion, into swizzled operand tiles (a
-//                second ring); tokens that were not copied become zeros;
+//   warps 4-7    K stream and
+//   warps 8-11   V stream.  Each stream feeds itself: its first thread
+//                issues the bulk copies (cp.async.bulk) of a tile's E4M3 K
+//                (V) rows from the paged cache into the stream's raw
+//                shared-memory ring, completion counted in bytes on an
+//                mbarrier, as soon as the stream has finished with the
+//                stage's previous tile; runs of tokens contiguous in a page
+//                move as one copy and tokens no query row may see are never
+//                copied.  The stream then decodes raw E4M3 -> exact fp16 with
+//                the hardware e4m3x2 -> f16x2 conversion into swizzled
+//                operand tiles of its own ring (tokens that were not copied
+//                become zeros).  K and V have separate rings because
+//                different MMAs free them: a K tile is free once its QK is
+//                done, a V tile only once its PV is;
 //   warp 12      TMEM allocation and UMMA issue (one elected thread);
 //   warps 0-3    softmax: read S from TMEM, online softmax with FP32 state,
 //                write P = P_hi + P_lo (two fp16 halves) back to TMEM in place
@@ -48,12 +54,15 @@ using namespace tc;
 
 constexpr int kT = 64;              // tokens per tile (16 microblocks in sparse mode)
 constexpr int kRows = 64;           // query vectors per CTA
+constexpr int kE = kT / 4;          // sparse entries per tile
 constexpr int kSoftmaxWarps = 4;
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 4;        // per stream
 constexpr int kDecThreads = 32 * kDecWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + kDecWarps;   // 12
-constexpr int kProdWarp = kMmaWarp + 1;               // 13
-constexpr int kThreads = 32 * (kProdWarp + 1);        // 448
+constexpr int kKDecWarp0 = kSoftmaxWarps;              // 4
+constexpr int kVDecWarp0 = kKDecWarp0 + kDecWarps;     // 8
+constexpr int kMmaWarp = kVDecWarp0 + kDecWarps;       // 12
+constexpr int kThreads = 32 * (kMmaWarp + 1);          // 416
+static_assert(kThreads == kTcThreads && kT == kTcTileTokens, "launch shape");
 constexpr float kTau = 8.0f;        // lazy-rescale threshold (base-2 units)
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 24;  // consecutive idle probes of the MMA issuer
@@ -61,41 +70,45 @@ constexpr int kMaxStages = 4;
 
 template <int D>
 struct Cfg {
-  static constexpr int kStages = (D == 256) ? 2 : 3;       // fp16 operand stages
-  static constexpr int kRaw = (D == 256) ? 3 : 4;          // raw E4M3 stages
-  static constexpr int kKVBytes = kT * D * 2;              // one K or V tile (fp16)
-  static constexpr int kStageBytes = 2 * kKVBytes;
-  static constexpr int kRawBytes = 2 * kT * D;             // raw K rows then raw V rows
-  static constexpr int kOffStages = 0;
-  static constexpr int kOffRaw = kOffStages + kStages * kStageBytes;
-  static constexpr int kOffMeta = kOffRaw + kRaw * kRawBytes;
+  static constexpr int kKStages = (D == 256) ? 3 : 4;      // fp16 K operand stages
+  static constexpr int kVStages = (D == 256) ? 2 : 3;      // fp16 V operand stages
+  static constexpr int kRaw = (D == 256) ? 2 : 4;          // raw E4M3 stages per stream
+  static constexpr int kOpBytes = kT * D * 2;              // one K or V operand tile (fp16)
+  static constexpr int kRawBytes = kT * D;                 // raw K or V rows of a tile
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKStages * kOpBytes;
+  static constexpr int kOffRawK = kOffV + kVStages * kOpBytes;
+  static constexpr int kOffRawV = kOffRawK + kRaw * kRawBytes;
+  static constexpr int kOffMeta = kOffRawV + kRaw * kRawBytes;
   static constexpr int kMetaBytes = 1024;
   static constexpr int kSmem = kOffMeta + kMetaBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColQ = 0;      // D/2 columns (fp16 pairs)
   static constexpr uint32_t kColS = 128;    // 2 x 64 columns; P(i) overwrites S(i)
   static constexpr uint32_t kColO = 256;    // D columns
-  static_assert(kStages <= kMaxStages && kRaw <= kMaxStages, "ring sizes");
+  static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages && kRaw <= kMaxStages, "ring sizes");
+  static_assert(kSmem <= 232448, "shared memory");
 };
 
 struct Meta {
-  uint64_t kv_full[kMaxStages];
-  uint64_t kv_empty[kMaxStages];
-  uint64_t raw_full[kMaxStages];
-  uint64_t raw_empty[kMaxStages];
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages];
+  uint64_t v_full[kMaxStages], v_empty[kMaxStages];
+  uint64_t rawk_full[kMaxStages], rawv_full[kMaxStages];
   uint64_t s_full[2];
   uint64_t pv_done[2];
-  uint64_t p_ready;
+  uint64_t p_ready[2];                  // per S/P buffer: a warp can run a tile ahead
   uint32_t tmem;
   uint32_t pad;
-  uint64_t valid[kMaxStages];           // per raw stage: tokens that were copied
-  uint32_t raw_masks[kMaxStages][16];   // sparse: entry masks of each raw stage's tile
-  uint32_t masks[kMaxStages][16];       // sparse: entry masks of each operand stage's tile
+  uint64_t validk[kMaxStages];          // per raw K stage: tokens that were copied
+  uint64_t validv[kMaxStages];          // the same for the raw V stage
+  uint32_t pmask[2][kE];                // sparse: entry masks of the tile each stream copies
   int32_t nrow[kRows];                  // dense: live length of each query vector; sparse: its query row
 };
+static_assert(sizeof(Meta) <= 1024, "meta block");
 
 // ---------------------------------------------------------------- TMEM 16xNb
 
+// (Each wrapper waits for its own access, as those in tc_ptx.cuh do.)
 // 16 lanes x 256 bits (8 columns) per repeat; thread t holds, per repeat g,
 // lanes (t/4) and (t/4 + 8), columns 8g + 2*(t%4) + {0, 1}, registers in the
 // order (lane t/4: col, col+1), (lane t/4+8: col, col+1).
@@ -103,7 +116,8 @@ __device__ __forceinline__ void ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
   asm volatile(
       "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
@@ -116,7 +130,8 @@ __device__ __forceinline__ void ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
 __device__ __forceinline__ void st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
@@ -133,13 +148,111 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
 
 // Exact E4M3 -> fp16 for two bytes (hardware conversion): dec(b) itself;
 // |dec| <= 448 and the subnormal quantum 2^-9 are both exact in fp16.
-__device__ __forceinline__ uint32_t cvt2(uint32_t w16) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(w16));
-  return r;
+// Four E4M3 bytes (little-endian in w) -> two fp16 pairs (bytes 0,1 and 2,3).
+__device__ __forceinline__ void cvt4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
-  return make_uint4(cvt2(a & 0xFFFFu), cvt2(a >> 16), cvt2(b & 0xFFFFu), cvt2(b >> 16));
+  uint4 r;
+  cvt4(a, r.x, r.y);
+  cvt4(b, r.z, r.w);
+  return r;
+}
+
+// Decode one raw tile (kT rows of D E4M3 bytes) into a swizzled fp16 operand
+// tile with the kDecThreads threads of a stream: column block db = d/64 holds
+// kT rows of 128 bytes; the 16-byte chunk c of row t sits at chunk position
+// c ^ (t % 8).  Thread lt always takes raw chunk c = lt % (D/16) of rows
+// lt / (D/16) + k * R (R = rows per pass of all threads), so every address
+// is a per-thread base plus a compile-time offset; all loads are issued
+// before the first conversion.  Rows whose bit in `valid` is clear were not
+// copied and become zeros.
+template <int D>
+__device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uint64_t valid, int lt) {
+  constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
+  constexpr int kR = kDecThreads / kChunks; // rows per pass
+  constexpr int kPer = kT / kR;             // chunks per thread
+  static_assert(kDecThreads % kChunks == 0 && kT % kR == 0, "decoder shape");
+  const int c = lt % kChunks, t0 = lt / kChunks;
+  const int db = c / 4;
+  const int h0 = (c % 4) * 2;  // first of the two 16-byte fp16 chunks
+  // alternate the order of the two stores between column blocks so the
+  // eight threads of a store phase hit eight different bank groups
+  const bool swap = (db & 1) != 0;
+  const int first = swap ? h0 + 1 : h0;
+  const int second = swap ? h0 : h0 + 1;
+  const uint8_t* src = raw + t0 * D + c * 16;
+  uint8_t* dst = op + db * (kT * 128) + t0 * 128;
+  const bool full = valid == ~0ull;
+  uint4 w[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    w[k] = (full || ((valid >> (t0 + k * kR)) & 1ull)) ? *reinterpret_cast<const uint4*>(src + k * kR * D)
+                                                      : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int sw = (t0 + k * kR) & 7;
+    uint8_t* row = dst + k * kR * 128;
+    const uint4 x0 = dec8(w[k].x, w[k].y), x1 = dec8(w[k].z, w[k].w);
+    *reinterpret_cast<uint4*>(row + ((first ^ sw) * 16)) = swap ? x1 : x0;
+    *reinterpret_cast<uint4*>(row + ((second ^ sw) * 16)) = swap ? x0 : x1;
+  }
+}
+
+// Issue the bulk copies of one tile's K (or V) rows into a raw stage and
+// return the set of token slots that were copied.  Dense: runs of tokens
+// contiguous in a page; sparse: the tokens of each entry that some query row
+// attends (the tile's masks, already checked, are in `masks`).
+template <int D, int MODE>
+__device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* cache, int64_t sb, int64_t st,
+                                              int64_t sh, int b, int g, int u0, int u1, int i, uint8_t* dst,
+                                              uint64_t* bar, const uint32_t* masks, bool report) {
+  uint64_t valid = 0ull;
+  if (MODE == FP8KV_MODE_DENSE) {
+    int t = 0;
+    while (t < kT) {
+      const int tok = u0 + i * kT + t;
+      if (tok >= u1) break;
+      const int page = tok / p.page_size, slot_in = tok % p.page_size;
+      const int blk = p.block_table[(int64_t)b * p.bt_stride + page];
+      const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
+      if (blk >= 0 && blk < p.num_kv_blocks) {
+        const uint8_t* src = cache + blk * sb + slot_in * st + g * sh;
+        // rows of consecutive slots are adjacent when the token stride is D
+        if (st == D) {
+          mbar_expect_tx(bar, run * D);
+          bulk_g2s(dst + t * D, src, run * D, bar);
+        } else {
+          for (int r = 0; r < run; ++r) {
+            mbar_expect_tx(bar, D);
+            bulk_g2s(dst + (t + r) * D, src + r * st, D, bar);
+          }
+        }
+        valid |= ((run == 64) ? ~0ull : ((1ull << run) - 1ull)) << t;
+      } else if (report) {
+        set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
+      }
+      t += run;
+    }
+  } else {
+    for (int el = 0; el < kE; ++el) {
+      const uint32_t mk = masks[el];
+      if (mk == 0u) continue;
+      const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + u0 + i * kE + el];
+      for (int tk = 0; tk < 4; ++tk) {
+        if ((mk & (0x11111111u << tk)) == 0u) continue;
+        const int t = el * 4 + tk;
+        mbar_expect_tx(bar, D);
+        bulk_g2s(dst + t * D, cache + blk * sb + tk * st + g * sh, D, bar);
+        valid |= 1ull << t;
+      }
+    }
+  }
+  return valid;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -147,8 +260,6 @@ __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   using C = Cfg<D>;
-  constexpr int kChunks = D / 16;                              // 16-byte raw chunks per token row
-  constexpr int kDecPerTile = kT * kChunks / kDecThreads;      // per decoder thread, per K (and per V)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Meta& mt = *reinterpret_cast<Meta*>(smem + C::kOffMeta);
@@ -181,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       U = min(max(U, 0), p.max_blocks);
     }
   }
-  const int unit = (MODE == FP8KV_MODE_DENSE) ? kT : kT / 4;
+  const int unit = (MODE == FP8KV_MODE_DENSE) ? kT : kE;
   int per = (U + p.S - 1) / p.S;
   per = (per + unit - 1) / unit * unit;
   const int u0 = s * per;
@@ -195,19 +306,24 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 
   // ---------------------------------------------------------- setup
   if (tid == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&mt.kv_full[i], kDecThreads);
-      mbar_init(&mt.kv_empty[i], 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&mt.k_full[i], kDecThreads);
+      mbar_init(&mt.k_empty[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&mt.v_full[i], kDecThreads);
+      mbar_init(&mt.v_empty[i], 1);
     }
     for (int i = 0; i < C::kRaw; ++i) {
-      mbar_init(&mt.raw_full[i], 1);
-      mbar_init(&mt.raw_empty[i], kDecThreads);
+      mbar_init(&mt.rawk_full[i], 1);
+      mbar_init(&mt.rawv_full[i], 1);
     }
     mbar_init(&mt.s_full[0], 1);
     mbar_init(&mt.s_full[1], 1);
     mbar_init(&mt.pv_done[0], 1);
     mbar_init(&mt.pv_done[1], 1);
-    mbar_init(&mt.p_ready, 32 * kSoftmaxWarps);
+    mbar_init(&mt.p_ready[0], 32 * kSoftmaxWarps);
+    mbar_init(&mt.p_ready[1], 32 * kSoftmaxWarps);
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -259,138 +375,72 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   __syncthreads();
   tc_fence_after();
 
-  if (warp == kProdWarp) {
-    // ======================================================== producer
-    if (lane == 0) {
-      bool ok = true;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int slot = i % C::kRaw;
-        if (i >= C::kRaw) {
-          if (!mbar_wait(&mt.raw_empty[slot], ((i / C::kRaw) - 1) & 1, kWaitLimit)) ok = false;
-        }
-        uint8_t* rK = smem + C::kOffRaw + slot * C::kRawBytes;
-        uint8_t* rV = rK + kT * D;
-        uint64_t* bar = &mt.raw_full[slot];
-        uint64_t valid = 0;
-        if (MODE == FP8KV_MODE_DENSE) {
-          int t = 0;
-          while (t < kT) {
-            const int tok = u0 + i * kT + t;
-            if (tok >= u1) break;
-            const int page = tok / p.page_size, slot_in = tok % p.page_size;
-            const int blk = p.block_table[(int64_t)b * p.bt_stride + page];
-            const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
-            if (blk < 0 || blk >= p.num_kv_blocks) {
-              set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
-              t += run;
-              continue;
+  if (warp >= kKDecWarp0 && warp < kMmaWarp) {
+    // ======================================================== K / V streams
+    const bool is_k = warp < kVDecWarp0;
+    const int lt = tid - 32 * (is_k ? kKDecWarp0 : kVDecWarp0);
+    const uint32_t grp_bar = is_k ? 1 : 2;  // named barrier of the stream's threads
+    const int n_stages = is_k ? C::kKStages : C::kVStages;
+    uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
+    uint64_t* op_full = is_k ? mt.k_full : mt.v_full;
+    uint64_t* op_empty = is_k ? mt.k_empty : mt.v_empty;
+    uint64_t* valid = is_k ? mt.validk : mt.validv;
+    const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+    const int64_t csb = is_k ? p.ksb : p.vsb, cst = is_k ? p.kst : p.vst, csh = is_k ? p.ksh : p.vsh;
+    uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
+    uint8_t* op_base = smem + (is_k ? C::kOffK : C::kOffV);
+    uint32_t* masks = mt.pmask[is_k ? 0 : 1];
+    // (first thread of the stream) bulk copies of tile i into its raw stage
+    auto issue = [&](int i) {
+      const int slot = i % C::kRaw;
+      if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
+        // entry masks of the tile; an entry with a bad block contributes nothing
+        for (int el = 0; el < kE; ++el) {
+          const int e = u0 + i * kE + el;
+          uint32_t mk = 0;
+          if (e < u1) {
+            mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
+            const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
+            if (mk != 0u && (blk < 0 || blk >= p.num_kv_blocks)) {
+              if (is_k) set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
+              mk = 0;
             }
-            const uint8_t* ks = p.k_cache + blk * p.ksb + slot_in * p.kst + g * p.ksh;
-            const uint8_t* vs = p.v_cache + blk * p.vsb + slot_in * p.vst + g * p.vsh;
-            // rows of consecutive slots are adjacent when the token stride is D
-            if (p.kst == D) {
-              mbar_expect_tx(bar, run * D);
-              bulk_g2s(rK + t * D, ks, run * D, bar);
-            } else {
-              for (int r = 0; r < run; ++r) {
-                mbar_expect_tx(bar, D);
-                bulk_g2s(rK + (t + r) * D, ks + r * p.kst, D, bar);
-              }
-            }
-            if (p.vst == D) {
-              mbar_expect_tx(bar, run * D);
-              bulk_g2s(rV + t * D, vs, run * D, bar);
-            } else {
-              for (int r = 0; r < run; ++r) {
-                mbar_expect_tx(bar, D);
-                bulk_g2s(rV + (t + r) * D, vs + r * p.vst, D, bar);
-              }
-            }
-            valid |= ((run == 64) ? ~0ull : ((1ull << run) - 1ull)) << t;
-            t += run;
           }
-        } else {
-          for (int el = 0; el < kT / 4; ++el) {
-            const int e = u0 + i * (kT / 4) + el;
-            uint32_t mk = 0;
-            if (e < u1) {
-              mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
-              const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-              if (mk != 0u && (blk < 0 || blk >= p.num_kv_blocks)) {
-                set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
-                mk = 0;
-              }
-              if (mk != 0u) {
-                // only tokens that at least one query row attends are copied
-                for (int tk = 0; tk < 4; ++tk) {
-                  if ((mk & (0x11111111u << tk)) == 0u) continue;
-                  const int t = el * 4 + tk;
-                  mbar_expect_tx(bar, 2 * D);
-                  bulk_g2s(rK + t * D, p.k_cache + blk * p.ksb + tk * p.kst + g * p.ksh, D, bar);
-                  bulk_g2s(rV + t * D, p.v_cache + blk * p.vsb + tk * p.vst + g * p.vsh, D, bar);
-                  valid |= 1ull << t;
-                }
-              }
-            }
-            mt.raw_masks[slot][el] = mk;
-          }
+          masks[el] = mk;
         }
-        mt.valid[slot] = valid;
-        mbar_arrive(bar);
       }
-      if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
+      valid[slot] = copy_rows<D, MODE>(p, cache, csb, cst, csh, b, g, u0, u1, i, raw_base + slot * C::kRawBytes,
+                                       &raw_full[slot], masks, is_k);
+      mbar_arrive(&raw_full[slot]);
+    };
+    if (lt == 0) {
+      for (int i = 0; i < C::kRaw && i < n_tiles; ++i) issue(i);
     }
+    // the stream's named barrier is an aligned barrier: the warp of the
+    // issuing thread must reach it converged
     __syncwarp();
-  } else if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
-    // ======================================================== decoders
-    const int lt = tid - 32 * kSoftmaxWarps;
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i % C::kRaw;
-      const int st = i % C::kStages;
-      if (!mbar_wait(&mt.raw_full[slot], (i / C::kRaw) & 1, kWaitLimit)) ok = false;
-      if (i >= C::kStages) {
-        if (!mbar_wait(&mt.kv_empty[st], ((i / C::kStages) - 1) & 1, kWaitLimit)) ok = false;
+      const int st = i % n_stages;
+      // raw rows arrived, and the operand stage is free (the MMA that read
+      // its previous tile is done)
+      if (!mbar_wait(&raw_full[slot], (i / C::kRaw) & 1, kWaitLimit)) ok = false;
+      if (i >= n_stages) {
+        if (!mbar_wait(&op_empty[st], ((i / n_stages) - 1) & 1, kWaitLimit)) ok = false;
       }
-      const uint8_t* rK = smem + C::kOffRaw + slot * C::kRawBytes;
-      const uint8_t* rV = rK + kT * D;
-      uint8_t* sK = smem + C::kOffStages + st * C::kStageBytes;
-      uint8_t* sV = sK + C::kKVBytes;
-      const uint64_t valid = mt.valid[slot];
-      if (MODE == FP8KV_MODE_SPARSE_PAGE4 && lt < 16) mt.masks[st][lt] = mt.raw_masks[slot][lt];
-      uint4 kw[kDecPerTile], vw[kDecPerTile];
-#pragma unroll
-      for (int j = 0; j < kDecPerTile; ++j) {
-        const int L = j * kDecThreads + lt;
-        const int t = L / kChunks, c = L % kChunks;
-        const bool ok_t = (valid >> t) & 1ull;
-        kw[j] = ok_t ? *reinterpret_cast<const uint4*>(rK + t * D + c * 16) : make_uint4(0, 0, 0, 0);
-        vw[j] = ok_t ? *reinterpret_cast<const uint4*>(rV + t * D + c * 16) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int j = 0; j < kDecPerTile; ++j) {
-        const int L = j * kDecThreads + lt;
-        const int t = L / kChunks, c = L % kChunks;
-        const int db = c / 4;
-        const int h0 = (c % 4) * 2;  // first of the two 16-byte fp16 chunks
-        // alternate the order of the two stores between column blocks so the
-        // eight threads of a store phase hit eight different bank groups
-        const bool swap = (db & 1) != 0;
-        const int first = swap ? h0 + 1 : h0;
-        const int second = swap ? h0 : h0 + 1;
-        uint8_t* rowK = sK + db * (kT * 128) + t * 128;
-        uint8_t* rowV = sV + db * (kT * 128) + t * 128;
-        const uint4 k0 = dec8(kw[j].x, kw[j].y), k1 = dec8(kw[j].z, kw[j].w);
-        const uint4 v0 = dec8(vw[j].x, vw[j].y), v1 = dec8(vw[j].z, vw[j].w);
-        const int sw = t & 7;
-        *reinterpret_cast<uint4*>(rowK + ((first ^ sw) * 16)) = swap ? k1 : k0;
-        *reinterpret_cast<uint4*>(rowK + ((second ^ sw) * 16)) = swap ? k0 : k1;
-        *reinterpret_cast<uint4*>(rowV + ((first ^ sw) * 16)) = swap ? v1 : v0;
-        *reinterpret_cast<uint4*>(rowV + ((second ^ sw) * 16)) = swap ? v0 : v1;
-      }
+      decode_tile<D>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
       fence_proxy_async_smem();
-      mbar_arrive(&mt.kv_full[st]);
-      mbar_arrive(&mt.raw_empty[slot]);
+      mbar_arrive(&op_full[st]);
+      if (i + C::kRaw < n_tiles) {
+        // the whole stream is done with the raw stage: refill it
+        named_bar(grp_bar, kDecThreads);
+        if (lt == 0) {
+          fence_proxy_async_smem();
+          issue(i + C::kRaw);
+        }
+        __syncwarp();
+      }
     }
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
@@ -401,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       bool ok = true;
       // Step i holds two independent chains: the QK of tile i and the PV of
       // tile i-1.  Whichever is ready first is issued first, so a PV never
-      // waits behind the decode of the next tile (the decoders in turn wait
-      // for that PV to free an operand stage).  Readiness is probed between
+      // waits behind the decode of the next K tile, nor a QK behind a V
+      // tile that is still being decoded.  Readiness is probed between
       // whole chains only: an mbarrier probe right after a UMMA stalls the
       // issuing thread for about the UMMA's latency.
       uint32_t spins = 0;
@@ -410,10 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         const int j = i - 1;
         bool qk_todo = i < n_tiles, pv_todo = i >= 1;
         while (qk_todo || pv_todo) {
-          if (pv_todo && mbar_test(&mt.p_ready, j & 1)) {
+          if (pv_todo && mbar_test(&mt.p_ready[j & 1], (j >> 1) & 1) &&
+              mbar_test(&mt.v_full[j % C::kVStages], (j / C::kVStages) & 1)) {
             tc_fence_after();
-            const int st = j % C::kStages;
-            const uint32_t sv = smem_u32(smem + C::kOffStages + st * C::kStageBytes + C::kKVBytes);
+            const int st = j % C::kVStages;
+            const uint32_t sv = smem_u32(smem + C::kOffV + st * C::kOpBytes);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk) {
               const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
@@ -421,20 +472,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
                      (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&mt.pv_done[j & 1]);
-            mma_commit(&mt.kv_empty[st]);
+            mma_commit(&mt.v_empty[st]);
             pv_todo = false;
             spins = 0;
-          } else if (qk_todo && mbar_test(&mt.kv_full[i % C::kStages], (i / C::kStages) & 1) &&
+          } else if (qk_todo && mbar_test(&mt.k_full[i % C::kKStages], (i / C::kKStages) & 1) &&
                      // S(i) overwrites the buffer that held P(i-2): PV(i-2) must be done
                      (i < 2 || mbar_test(&mt.pv_done[i & 1], ((i - 2) >> 1) & 1))) {
             tc_fence_after();
-            const uint32_t sk = smem_u32(smem + C::kOffStages + (i % C::kStages) * C::kStageBytes);
+            const uint32_t sk = smem_u32(smem + C::kOffK + (i % C::kKStages) * C::kOpBytes);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
               mma_ts(tmem + C::kColS + (i & 1) * kT, tmem + C::kColQ + kk * 8, bd, idesc_qk, kk > 0);
             }
             mma_commit(&mt.s_full[i & 1]);
+            mma_commit(&mt.k_empty[i % C::kKStages]);
             qk_todo = false;
             spins = 0;
           } else if (++spins > kSpinLimit) {
@@ -461,11 +513,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     for (int i = 0; i < n_tiles; ++i) {
       if (!mbar_wait(&mt.s_full[i & 1], (i >> 1) & 1, kWaitLimit)) ok = false;
       tc_fence_after();
-      const int st = i % C::kStages;
-      if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
-        // the tile's masks were published by the decoders with kv_full[st]
-        if (!mbar_wait(&mt.kv_full[st], (i / C::kStages) & 1, kWaitLimit)) ok = false;
-      }
       if (warp_live) {
         uint32_t sr[32];
         ld_16x256b_x8(tmem + C::kColS + (i & 1) * kT + lane_off, sr);
@@ -489,17 +536,25 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
               }
           }
         } else {
+          // columns 8gq + 2(lane%4) + {0,1} lie in entry 2gq + (lane%4)/2 of
+          // the tile; an entry whose block is out of range attends nothing
           vis = 0;
 #pragma unroll
-          for (int gq = 0; gq < 8; ++gq)
+          for (int gq = 0; gq < 8; ++gq) {
+            const int ent = u0 + i * kE + 2 * gq + ((lane & 3) >> 1);
+            uint32_t mk = 0u;
+            if (ent < u1) {
+              mk = p.entry_mask[(int64_t)b * p.entry_stride + ent];
+              const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + ent];
+              if (blk < 0 || blk >= p.num_kv_blocks) mk = 0u;
+            }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int col = 8 * gq + 2 * (lane & 3) + e;
-              const int ent = u0 + i * (kT / 4) + col / 4;
-              const uint32_t mk = (ent < u1) ? mt.masks[st][col / 4] : 0u;
-              vis |= ((n_a >= 0) ? ((mk >> (4 * n_a + (col & 3))) & 1u) : 0u) << (2 * gq + e);
-              vis |= ((n_b >= 0) ? ((mk >> (4 * n_b + (col & 3))) & 1u) : 0u) << (16 + 2 * gq + e);
+              const int pos = (2 * (lane & 3) + e) & 3;
+              vis |= ((n_a >= 0) ? ((mk >> (4 * n_a + pos)) & 1u) : 0u) << (2 * gq + e);
+              vis |= ((n_b >= 0) ? ((mk >> (4 * n_b + pos)) & 1u) : 0u) << (16 + 2 * gq + e);
             }
+          }
         }
         float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
@@ -581,7 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(&mt.p_ready);
+      // (one barrier per buffer: a warp without query vectors may already
+      // be on the next tile while another still writes this one's P)
+      mbar_arrive(&mt.p_ready[i & 1]);
     }
     // ------------------------------------------------------ epilogue
     if (!mbar_wait(&mt.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, kWaitLimit)) ok = false;
