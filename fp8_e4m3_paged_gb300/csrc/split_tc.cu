@@ -3,18 +3,17 @@
 //
 // Per CTA: one partition (a contiguous token range, or entry range in the
 // sparse microblock mode) of one (request, KV head, row chunk).  Warp roles:
-//   warps 4-7    K stream and
-//   warps 8-11   V stream.  Each stream feeds itself: its first thread
-//                issues the bulk copies (cp.async.bulk) of a tile's E4M3 K
-//                (V) rows from the paged cache into the stream's raw
-//                shared-memory ring, completion counted in bytes on an
-//                mbarrier, as soon as the stream has finished with the
-//                stage's previous tile; runs of tokens contiguous in a page
-//                move as one copy and tokens no query row may see are never
-//                copied.  The stream then decodes raw E4M3 -> exact fp16 with
-//                the hardware e4m3x2 -> f16x2 conversion into swizzled
-//                operand tiles of its own ring (tokens that were not copied
-//                become zeros).  K and V have separate rings because
+//   warps 13, 14 producers (one thread each, K and V): bulk copies
+//                (cp.async.bulk) of a tile's E4M3 K (V) rows from the paged
+//                cache into that stream's raw shared-memory ring, completion
+//                counted in bytes on an mbarrier; runs of tokens contiguous
+//                in a page move as one copy and tokens no query row may see
+//                are never copied;
+//   warps 4-7    K decoders and
+//   warps 8-11   V decoders: raw E4M3 -> exact fp16 with the hardware
+//                e4m3x2 -> f16x2 conversion into swizzled operand tiles of
+//                the stream's ring (tokens that were not copied become
+//                zeros).  K and V have separate rings and producers because
 //                different MMAs free them: a K tile is free once its QK is
 //                done, a V tile only once its PV is;
 //   warp 12      TMEM allocation and UMMA issue (one elected thread);
@@ -22,13 +21,17 @@
 //                write P = P_hi + P_lo (two fp16 halves) back to TMEM in place
 //                of S, rescale O when the running max jumps, epilogue.
 // Per 64-token tile:
-//   QK:  S[128 x 64] = Q[128 x D] . K^T   (M=128, A = Q resident in TMEM,
-//        B = K tile from shared memory, K-major).  Query vector 16w+j
-//        (j < 16) sits in TMEM lane 32w+j; lanes 32w+16..31 are zero rows.
+//   QK:  S[64 x 64] = Q[64 x D] . K^T   (UMMA M=64: A = Q resident in
+//        shared memory, B = K tile from shared memory, both K-major).  Query
+//        vector 16w+j (j < 16) lands in TMEM lane 32w+j.
 //   PV:  O[128 x D] += P[128 x 64] . V[64 x D]  (M=128, A from TMEM, B = V
 //        tile MN-major).  P_hi of vector 16w+j sits in lane 32w+j and its
 //        P_lo twin in lane 32w+16+j, so one MMA accumulates both halves of
 //        the probability split; the epilogue adds the two accumulator rows.
+// TMEM: four S/P buffers of 64 columns (P(i) overwrites S(i) in buffer i%4,
+// hi in the lanes the M=64 QK writes, lo in the 16 lanes above) and O.  With
+// four buffers the QK of tile i+4 is the first to wait for the PV of tile i,
+// so QK, softmax and PV of neighbouring tiles overlap.
 // The hi/lo split keeps probabilities to ~22 bits ("compensated
 // probabilities"); the FP32 partition numerator, max and sum follow the FP32
 // state contract ("DFlash2 E4M3 attention with FP32 state", intro paragraph
@@ -61,21 +64,27 @@ constexpr int kDecThreads = 32 * kDecWarps;
 constexpr int kKDecWarp0 = kSoftmaxWarps;              // 4
 constexpr int kVDecWarp0 = kKDecWarp0 + kDecWarps;     // 8
 constexpr int kMmaWarp = kVDecWarp0 + kDecWarps;       // 12
-constexpr int kThreads = 32 * (kMmaWarp + 1);          // 416
+constexpr int kProdWarp = kMmaWarp + 1;                // 13 (K), 14 (V)
+constexpr int kSchedWarp = kProdWarp + 2;              // 15
+constexpr int kThreads = 32 * (kSchedWarp + 1);        // 512
 static_assert(kThreads == kTcThreads && kT == kTcTileTokens, "launch shape");
 constexpr float kTau = 8.0f;        // lazy-rescale threshold (base-2 units)
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kSpinLimit = 1u << 24;  // consecutive idle probes of the MMA issuer
+constexpr uint32_t kSpinLimit = 1u << 24;  // consecutive idle polls of the scheduler / issuer
 constexpr int kMaxStages = 4;
+constexpr int kSBuf = 4;            // S/P buffers in TMEM
+constexpr int kCmdRing = 8;         // scheduler -> MMA issuer command ring
 
 template <int D>
 struct Cfg {
-  static constexpr int kKStages = (D == 256) ? 3 : 4;      // fp16 K operand stages
+  static constexpr int kKStages = (D == 256) ? 2 : 3;      // fp16 K operand stages
   static constexpr int kVStages = (D == 256) ? 2 : 3;      // fp16 V operand stages
   static constexpr int kRaw = (D == 256) ? 2 : 4;          // raw E4M3 stages per stream
+  static constexpr int kQBytes = kRows * D * 2;            // Q tile (fp16, swizzled)
   static constexpr int kOpBytes = kT * D * 2;              // one K or V operand tile (fp16)
   static constexpr int kRawBytes = kT * D;                 // raw K or V rows of a tile
-  static constexpr int kOffK = 0;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kOpBytes;
   static constexpr int kOffRawK = kOffV + kVStages * kOpBytes;
   static constexpr int kOffRawV = kOffRawK + kRaw * kRawBytes;
@@ -83,8 +92,7 @@ struct Cfg {
   static constexpr int kMetaBytes = 1024;
   static constexpr int kSmem = kOffMeta + kMetaBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColQ = 0;      // D/2 columns (fp16 pairs)
-  static constexpr uint32_t kColS = 128;    // 2 x 64 columns; P(i) overwrites S(i)
+  static constexpr uint32_t kColS = 0;      // kSBuf x 64 columns; P(i) overwrites S(i)
   static constexpr uint32_t kColO = 256;    // D columns
   static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages && kRaw <= kMaxStages, "ring sizes");
   static_assert(kSmem <= 232448, "shared memory");
@@ -94,11 +102,13 @@ struct Meta {
   uint64_t k_full[kMaxStages], k_empty[kMaxStages];
   uint64_t v_full[kMaxStages], v_empty[kMaxStages];
   uint64_t rawk_full[kMaxStages], rawv_full[kMaxStages];
-  uint64_t s_full[2];
-  uint64_t pv_done[2];
-  uint64_t p_ready[2];                  // per S/P buffer: a warp can run a tile ahead
+  uint64_t rawk_empty[kMaxStages], rawv_empty[kMaxStages];
+  uint64_t s_full[kSBuf];               // per S/P buffer
+  uint64_t pv_done[kSBuf];
+  uint64_t p_ready[kSBuf];              // per buffer: a warp can run tiles ahead
   uint32_t tmem;
-  uint32_t pad;
+  uint32_t cmd_head, cmd_tail;          // commands published / issued
+  uint32_t cmd[kCmdRing];               // (1 << 16 | tile): PV, tile: QK
   uint64_t validk[kMaxStages];          // per raw K stage: tokens that were copied
   uint64_t validv[kMaxStages];          // the same for the raw V stage
   uint32_t pmask[2][kE];                // sparse: entry masks of the tile each stream copies
@@ -317,13 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     for (int i = 0; i < C::kRaw; ++i) {
       mbar_init(&mt.rawk_full[i], 1);
       mbar_init(&mt.rawv_full[i], 1);
+      mbar_init(&mt.rawk_empty[i], kDecThreads);
+      mbar_init(&mt.rawv_empty[i], kDecThreads);
     }
-    mbar_init(&mt.s_full[0], 1);
-    mbar_init(&mt.s_full[1], 1);
-    mbar_init(&mt.pv_done[0], 1);
-    mbar_init(&mt.pv_done[1], 1);
-    mbar_init(&mt.p_ready[0], 32 * kSoftmaxWarps);
-    mbar_init(&mt.p_ready[1], 32 * kSoftmaxWarps);
+    for (int i = 0; i < kSBuf; ++i) {
+      mbar_init(&mt.s_full[i], 1);
+      mbar_init(&mt.pv_done[i], 1);
+      mbar_init(&mt.p_ready[i], 32 * kSoftmaxWarps);
+    }
+    mt.cmd_head = 0;
+    mt.cmd_tail = 0;
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -343,82 +356,85 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   tc_fence_after();
   const uint32_t tmem = mt.tmem;
 
-  if (warp < kSoftmaxWarps) {
-    // Q -> TMEM: lane 32w+j (j < 16) holds query vector 16w+j as fp16 pairs
-    // along the columns; lanes 32w+16..31 are zero rows.
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    const int qi = 16 * warp + lane;
-    const bool has = (lane < 16) && (qi < RC);
-    const uint16_t* qp = nullptr;
-    if (has) {
-      const int rowi = row0 + qi;
+  // Q rows -> swizzled K-major tile in shared memory (rows >= RC are zero)
+  uint8_t* sQ = smem + C::kOffQ;
+  for (int idx = tid; idx < kRows * (D / 8); idx += kThreads) {
+    const int i = idx / (D / 8), c8 = idx % (D / 8);  // row, 8-element chunk
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (i < RC) {
+      const int rowi = row0 + i;
       const int r = rowi / p.G, h = g * p.G + rowi % p.G;
-      qp = p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D;
+      v = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D + c8 * 8);
     }
-#pragma unroll 1
-    for (int c0 = 0; c0 < D / 2; c0 += 16) {
-      uint32_t v[16];
-#pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (has) x = *reinterpret_cast<const uint4*>(qp + 2 * (c0 + j));
-        v[j] = x.x;
-        v[j + 1] = x.y;
-        v[j + 2] = x.z;
-        v[j + 3] = x.w;
-      }
-      tmem_st16(tmem + C::kColQ + lane_off + c0, v);
-    }
-    tmem_st_wait();
+    const int db = c8 / 8, ch = c8 % 8;
+    *reinterpret_cast<uint4*>(sQ + db * (kRows * 128) + i * 128 + ((ch ^ (i & 7)) * 16)) = v;
   }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  if (warp >= kKDecWarp0 && warp < kMmaWarp) {
-    // ======================================================== K / V streams
-    const bool is_k = warp < kVDecWarp0;
-    const int lt = tid - 32 * (is_k ? kKDecWarp0 : kVDecWarp0);
-    const uint32_t grp_bar = is_k ? 1 : 2;  // named barrier of the stream's threads
-    const int n_stages = is_k ? C::kKStages : C::kVStages;
-    uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
-    uint64_t* op_full = is_k ? mt.k_full : mt.v_full;
-    uint64_t* op_empty = is_k ? mt.k_empty : mt.v_empty;
-    uint64_t* valid = is_k ? mt.validk : mt.validv;
-    const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
-    const int64_t csb = is_k ? p.ksb : p.vsb, cst = is_k ? p.kst : p.vst, csh = is_k ? p.ksh : p.vsh;
-    uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
-    uint8_t* op_base = smem + (is_k ? C::kOffK : C::kOffV);
-    uint32_t* masks = mt.pmask[is_k ? 0 : 1];
-    // (first thread of the stream) bulk copies of tile i into its raw stage
-    auto issue = [&](int i) {
-      const int slot = i % C::kRaw;
-      if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
-        // entry masks of the tile; an entry with a bad block contributes nothing
-        for (int el = 0; el < kE; ++el) {
-          const int e = u0 + i * kE + el;
-          uint32_t mk = 0;
-          if (e < u1) {
-            mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
-            const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-            if (mk != 0u && (blk < 0 || blk >= p.num_kv_blocks)) {
+  if (warp == kProdWarp || warp == kProdWarp + 1) {
+    // ======================================================== producers
+    if (lane == 0) {
+      const bool is_k = warp == kProdWarp;
+      uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
+      uint64_t* raw_empty = is_k ? mt.rawk_empty : mt.rawv_empty;
+      uint64_t* valid = is_k ? mt.validk : mt.validv;
+      const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+      const int64_t csb = is_k ? p.ksb : p.vsb, cst = is_k ? p.kst : p.vst, csh = is_k ? p.ksh : p.vsh;
+      uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
+      uint32_t* masks = mt.pmask[is_k ? 0 : 1];
+      bool ok = true;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int slot = i % C::kRaw;
+        if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
+          // entry masks of the tile (all loads first); an entry with a bad
+          // block contributes nothing
+          uint32_t mk[kE];
+          int bk[kE];
+#pragma unroll
+          for (int el = 0; el < kE; ++el) {
+            const int e = u0 + i * kE + el;
+            mk[el] = (e < u1) ? p.entry_mask[(int64_t)b * p.entry_stride + e] : 0u;
+            bk[el] = (e < u1) ? p.entry_tbl[(int64_t)b * p.entry_stride + e] : 0;
+          }
+#pragma unroll
+          for (int el = 0; el < kE; ++el) {
+            if (mk[el] != 0u && (bk[el] < 0 || bk[el] >= p.num_kv_blocks)) {
               if (is_k) set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
-              mk = 0;
+              mk[el] = 0u;
             }
           }
-          masks[el] = mk;
+          // the masks are read only by this thread, after the stage is free
+          if (i >= C::kRaw) {
+            if (!mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, kWaitLimit)) ok = false;
+          }
+#pragma unroll
+          for (int el = 0; el < kE; ++el) masks[el] = mk[el];
+        } else if (i >= C::kRaw) {
+          // the raw stage is free once the decoders took its previous tile
+          if (!mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, kWaitLimit)) ok = false;
         }
+        valid[slot] = copy_rows<D, MODE>(p, cache, csb, cst, csh, b, g, u0, u1, i,
+                                         raw_base + slot * C::kRawBytes, &raw_full[slot], masks, is_k);
+        mbar_arrive(&raw_full[slot]);
       }
-      valid[slot] = copy_rows<D, MODE>(p, cache, csb, cst, csh, b, g, u0, u1, i, raw_base + slot * C::kRawBytes,
-                                       &raw_full[slot], masks, is_k);
-      mbar_arrive(&raw_full[slot]);
-    };
-    if (lt == 0) {
-      for (int i = 0; i < C::kRaw && i < n_tiles; ++i) issue(i);
+      if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     }
-    // the stream's named barrier is an aligned barrier: the warp of the
-    // issuing thread must reach it converged
     __syncwarp();
+  } else if (warp >= kKDecWarp0 && warp < kMmaWarp) {
+    // ======================================================== decoders
+    const bool is_k = warp < kVDecWarp0;
+    const int lt = tid - 32 * (is_k ? kKDecWarp0 : kVDecWarp0);
+    const int n_stages = is_k ? C::kKStages : C::kVStages;
+    uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
+    uint64_t* raw_empty = is_k ? mt.rawk_empty : mt.rawv_empty;
+    uint64_t* op_full = is_k ? mt.k_full : mt.v_full;
+    uint64_t* op_empty = is_k ? mt.k_empty : mt.v_empty;
+    const uint64_t* valid = is_k ? mt.validk : mt.validv;
+    const uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
+    uint8_t* op_base = smem + (is_k ? C::kOffK : C::kOffV);
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i % C::kRaw;
@@ -432,66 +448,99 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       decode_tile<D>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
       fence_proxy_async_smem();
       mbar_arrive(&op_full[st]);
-      if (i + C::kRaw < n_tiles) {
-        // the whole stream is done with the raw stage: refill it
-        named_bar(grp_bar, kDecThreads);
-        if (lt == 0) {
-          fence_proxy_async_smem();
-          issue(i + C::kRaw);
-        }
-        __syncwarp();
-      }
+      mbar_arrive(&raw_empty[slot]);
     }
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
+    // Issues, in order, the chains the scheduler publishes.  It never probes
+    // an mbarrier (a probe by the issuing thread waits until its outstanding
+    // UMMAs have drained); the command ring is read with plain shared-memory
+    // acquire loads.
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16_f32(128, kT, false, false);
+      const uint32_t idesc_qk = idesc_f16_f32(64, kT, false, false);
+      const uint32_t sq = smem_u32(smem + C::kOffQ);
       const uint32_t idesc_pv = idesc_f16_f32(128, D, false, true);
       bool ok = true;
-      // Step i holds two independent chains: the QK of tile i and the PV of
-      // tile i-1.  Whichever is ready first is issued first, so a PV never
-      // waits behind the decode of the next K tile, nor a QK behind a V
-      // tile that is still being decoded.  Readiness is probed between
-      // whole chains only: an mbarrier probe right after a UMMA stalls the
-      // issuing thread for about the UMMA's latency.
-      uint32_t spins = 0;
+      const uint32_t n_cmd = 2u * (uint32_t)n_tiles;
+      for (uint32_t c = 0; c < n_cmd && ok; ++c) {
+        uint32_t spins = 0;
+        while (ld_acquire_u32(&mt.cmd_head) <= c) {
+          if (++spins > kSpinLimit) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        const uint32_t cmd = mt.cmd[c % kCmdRing];
+        tc_fence_after();
+        if (cmd >> 16) {
+          // PV(j): O += P(j) . V(j)
+          const int j = (int)(cmd & 0xFFFFu);
+          const int st = j % C::kVStages;
+          const uint32_t sv = smem_u32(smem + C::kOffV + st * C::kOpBytes);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk) {
+            const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
+            mma_ts(tmem + C::kColO, tmem + C::kColS + (j % kSBuf) * kT + kk * 8, bd, idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&mt.pv_done[j % kSBuf]);
+          mma_commit(&mt.v_empty[st]);
+        } else {
+          // QK(i): S(i) = Q . K(i)^T
+          const int i = (int)cmd;
+          const uint32_t sk = smem_u32(smem + C::kOffK + (i % C::kKStages) * C::kOpBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
+            const uint64_t ad = smem_desc(sq + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSw128);
+            mma_ss(tmem + C::kColS + (i % kSBuf) * kT, ad, bd, idesc_qk, kk > 0);
+          }
+          mma_commit(&mt.s_full[i % kSBuf]);
+          mma_commit(&mt.k_empty[i % C::kKStages]);
+        }
+        st_release_u32(&mt.cmd_tail, c + 1);
+      }
+      if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kSchedWarp) {
+    // ======================================================== scheduler
+    // Step i holds two independent chains: the QK of tile i and the PV of
+    // tile i-1.  Whichever is ready first is published first, so a PV never
+    // waits behind the decode of the next K tile, nor a QK behind a V tile
+    // still being decoded or a softmax still running.
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t head = 0, spins = 0;
       for (int i = 0; i <= n_tiles && ok; ++i) {
         const int j = i - 1;
         bool qk_todo = i < n_tiles, pv_todo = i >= 1;
-        while (qk_todo || pv_todo) {
-          if (pv_todo && mbar_test(&mt.p_ready[j & 1], (j >> 1) & 1) &&
-              mbar_test(&mt.v_full[j % C::kVStages], (j / C::kVStages) & 1)) {
-            tc_fence_after();
-            const int st = j % C::kVStages;
-            const uint32_t sv = smem_u32(smem + C::kOffV + st * C::kOpBytes);
-#pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk) {
-              const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
-              mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * kT + kk * 8, bd, idesc_pv,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+        while ((qk_todo || pv_todo) && ok) {
+          uint32_t cmd = 0;
+          bool have = false;
+          if (head - ld_acquire_u32(&mt.cmd_tail) < (uint32_t)kCmdRing) {
+            if (pv_todo && mbar_test(&mt.p_ready[j % kSBuf], (j / kSBuf) & 1) &&
+                mbar_test(&mt.v_full[j % C::kVStages], (j / C::kVStages) & 1)) {
+              cmd = (1u << 16) | (uint32_t)j;
+              pv_todo = false;
+              have = true;
+            } else if (qk_todo && mbar_test(&mt.k_full[i % C::kKStages], (i / C::kKStages) & 1) &&
+                       // S(i) overwrites the buffer that held P(i-4): PV(i-4) must be done
+                       (i < kSBuf || mbar_test(&mt.pv_done[i % kSBuf], ((i / kSBuf) - 1) & 1))) {
+              cmd = (uint32_t)i;
+              qk_todo = false;
+              have = true;
             }
-            mma_commit(&mt.pv_done[j & 1]);
-            mma_commit(&mt.v_empty[st]);
-            pv_todo = false;
-            spins = 0;
-          } else if (qk_todo && mbar_test(&mt.k_full[i % C::kKStages], (i / C::kKStages) & 1) &&
-                     // S(i) overwrites the buffer that held P(i-2): PV(i-2) must be done
-                     (i < 2 || mbar_test(&mt.pv_done[i & 1], ((i - 2) >> 1) & 1))) {
-            tc_fence_after();
-            const uint32_t sk = smem_u32(smem + C::kOffK + (i % C::kKStages) * C::kOpBytes);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-              mma_ts(tmem + C::kColS + (i & 1) * kT, tmem + C::kColQ + kk * 8, bd, idesc_qk, kk > 0);
-            }
-            mma_commit(&mt.s_full[i & 1]);
-            mma_commit(&mt.k_empty[i % C::kKStages]);
-            qk_todo = false;
+          }
+          if (have) {
+            mt.cmd[head % kCmdRing] = cmd;
+            st_release_u32(&mt.cmd_head, head + 1);
+            ++head;
             spins = 0;
           } else if (++spins > kSpinLimit) {
             ok = false;
-            break;
           }
         }
       }
@@ -511,11 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     const int n_a = mt.nrow[ra], n_b = mt.nrow[rb];
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      if (!mbar_wait(&mt.s_full[i & 1], (i >> 1) & 1, kWaitLimit)) ok = false;
+      if (!mbar_wait(&mt.s_full[i % kSBuf], (i / kSBuf) & 1, kWaitLimit)) ok = false;
       tc_fence_after();
       if (warp_live) {
         uint32_t sr[32];
-        ld_16x256b_x8(tmem + C::kColS + (i & 1) * kT + lane_off, sr);
+        ld_16x256b_x8(tmem + C::kColS + (i % kSBuf) * kT + lane_off, sr);
         tmem_ld_wait();
         // visibility of this thread's 16 columns for rows ra (bits 0..15) and rb (16..31)
         uint32_t vis;
@@ -610,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 
         if (__any_sync(0xffffffffu, resc_a || resc_b)) {
           // O must hold every earlier tile before it is rescaled: wait PV(i-1)
-          if (!mbar_wait(&mt.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimit)) ok = false;
+          if (!mbar_wait(&mt.pv_done[(i - 1) % kSBuf], ((i - 1) / kSBuf) & 1, kWaitLimit)) ok = false;
           tc_fence_after();
           // thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16 (the
           // P_hi row for lane < 16, its P_lo twin above); the alpha of vector
@@ -630,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
           }
         }
         // P(i) replaces S(i) in its buffer: hi in lanes 32w+0..15, lo 16 above
-        const uint32_t pcol = tmem + C::kColS + (i & 1) * kT + lane_off;
+        const uint32_t pcol = tmem + C::kColS + (i % kSBuf) * kT + lane_off;
         st_16x128b_x8(pcol, ph);
         st_16x128b_x8(pcol + (16u << 16), pl);
         tmem_st_wait();
@@ -638,10 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       tc_fence_before();
       // (one barrier per buffer: a warp without query vectors may already
       // be on the next tile while another still writes this one's P)
-      mbar_arrive(&mt.p_ready[i & 1]);
+      mbar_arrive(&mt.p_ready[i % kSBuf]);
     }
     // ------------------------------------------------------ epilogue
-    if (!mbar_wait(&mt.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, kWaitLimit)) ok = false;
+    if (!mbar_wait(&mt.pv_done[(n_tiles - 1) % kSBuf], ((n_tiles - 1) / kSBuf) & 1, kWaitLimit)) ok = false;
     tc_fence_after();
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     if (warp_live) {
