@@ -1,9 +1,10 @@
 """Pins from the pages' printed facts, and a check that the pins have teeth.
 
 * QSA mask rule (tests/golden/qsa_mask_rule.json): under the bit layout
-  "bit 4r+t = row r sees token t", the pages' null-block fix rule
-  (mask & (0x11111111 << t)) != 0 must coincide with "token t is seen by some
-  row", and the oracle's visible sets must follow the fixture row by row.
+  "bit 4r+t = row r sees token t", the null-block fix's test (some mask bit
+  at a position congruent to t modulo 4 is set) must coincide with "token t
+  is seen by some row", and the oracle's visible sets must follow the
+  fixture row by row.
 * FP16 output-rounding floor: rounding the FP64 output to fp16 costs a
   relative L2 of about 2.03e-4 ("DFlash2 E4M3 attention with FP32 state",
   results: the FP64 reference gives an FP16 rounding floor of 0.000203267).
