@@ -5,7 +5,7 @@
 //
 // written as fp16 with round-to-nearest-even.  A query vector whose total L is
 // 0 (dead row, or nothing visible) gets +0.0.  Partitions with l_s = 0 are
-// skipped by selection, so their numerators are never read.  The partition
+// dropped by selection, so their numerators are never used.  The partition
 // maxima are integers (base-2 units), so every w_s is an exact power of two
 // ("DFlash2 E4M3 attention with FP32 state", intro paragraph 4: FP32
 // combination, FP16 final activation; "Qwen4Exp: fp8_e4m3 main KV cache on
@@ -13,10 +13,10 @@
 //
 // One CTA per (query vector, 64-wide slice of D); its 256 threads are 16
 // partition lanes x 16 float4 columns.  The kernel is latency-bound (a few
-// MB in total), so it makes two dependent trips to memory: the (m, l) pairs
-// of all partitions (held in registers for the weights), then every
-// numerator a lane needs, all loads issued before the first FMA.  The lanes
-// are reduced in shared memory in a fixed order.
+// MB in total), so the (m, l) pairs of all partitions and the numerators a
+// lane needs (up to NB per lane) are loaded in one trip to memory, before
+// the weights are known.  The lanes are reduced in shared memory in a fixed
+// order.
 #include <cstdint>
 
 #include <cuda_fp16.h>
@@ -33,7 +33,7 @@ constexpr int SL = 16;      // partition lanes
 constexpr int DW = 64;      // d slice per CTA
 constexpr int MAXS = 1024;  // partitions whose weights are staged per pass
 constexpr int KR = MAXS / CT;  // (m, l) pairs a thread holds
-constexpr int NB = 8;       // numerator loads in flight per lane
+constexpr int NB = 12;      // numerator loads in flight per lane (S <= 192 in one trip)
 
 __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   __shared__ float red_m[CT / 32];
@@ -56,78 +56,96 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = p.S;
 
-  // global max over live partitions; the first MAXS pairs stay in registers
-  float mv[KR], lv[KR];
-  float M = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < KR; ++k) {
-    const int s = tid + k * CT;
-    mv[k] = -INFINITY;
-    lv[k] = 0.f;
-    if (s < S) {
-      const float2 v = ml[s * sstride];
-      mv[k] = v.x;
-      lv[k] = v.y;
-      if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
-  }
-  for (int s = tid + MAXS; s < S; s += CT) {
-    const float2 v = ml[s * sstride];
-    if (v.y > 0.f) M = fmaxf(M, v.x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red_m[warp] = M;
-  __syncthreads();
-  M = red_m[0];
-#pragma unroll
-  for (int k = 1; k < CT / 32; ++k) M = fmaxf(M, red_m[k]);
-
   const int sl = tid / (DW / 4), c4 = tid % (DW / 4);
+  const float* acc = p.partial + base * D + slice * DW + c4 * 4;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  const float* acc = p.partial + base * D + slice * DW + c4 * 4;
-  for (int s0 = 0; s0 < S && M != -INFINITY; s0 += MAXS) {
+  for (int s0 = 0; s0 < S; s0 += MAXS) {
     const int ns = min(MAXS, S - s0);
-    if (s0 > 0) __syncthreads();
+    // one trip to memory: the (m, l) pairs of this pass and, speculatively,
+    // the numerators this lane will need (a dead partition's numerator may
+    // hold anything: it is dropped by selection below, never multiplied)
+    float mv[KR], lv[KR];
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int kk = tid + k * CT;
+      mv[k] = -INFINITY;
+      lv[k] = 0.f;
+      if (kk < ns) {
+        const float2 v = ml[(s0 + kk) * sstride];
+        mv[k] = v.x;
+        lv[k] = v.y;
+      }
+    }
+    float4 a[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int k = sl + j * SL;
+      a[j] = (k < ns) ? *reinterpret_cast<const float4*>(acc + (int64_t)(s0 + k) * sstride * D)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (s0 == 0) {
+      // global max over live partitions (later passes re-read their pairs)
+      float M0 = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KR; ++k)
+        if (lv[k] > 0.f) M0 = fmaxf(M0, mv[k]);
+      for (int s = tid + MAXS; s < S; s += CT) {
+        const float2 v = ml[s * sstride];
+        if (v.y > 0.f) M0 = fmaxf(M0, v.x);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M0 = fmaxf(M0, __shfl_xor_sync(0xffffffffu, M0, off));
+      if (lane == 0) red_m[warp] = M0;
+    } else {
+      __syncthreads();  // the previous pass is done with s_w / s_l
+    }
+    __syncthreads();
+    float M = red_m[0];
+#pragma unroll
+    for (int k = 1; k < CT / 32; ++k) M = fmaxf(M, red_m[k]);
+    if (M == -INFINITY) break;  // nothing visible for this vector
 #pragma unroll
     for (int k = 0; k < KR; ++k) {
       const int kk = tid + k * CT;
       if (kk < ns) {
-        float m_s, l_s;
-        if (s0 == 0) {
-          m_s = mv[k];
-          l_s = lv[k];
-        } else {
-          const float2 v = ml[(s0 + kk) * sstride];
-          m_s = v.x;
-          l_s = v.y;
-        }
-        const bool live = l_s > 0.f;
-        s_w[kk] = live ? exp2_int(m_s - M) : 0.f;  // integer maxima: exact
-        s_l[kk] = live ? l_s : 0.f;
+        const bool live = lv[k] > 0.f;
+        s_w[kk] = live ? exp2_int(mv[k] - M) : 0.f;  // integer maxima: exact
+        s_l[kk] = live ? lv[k] : 0.f;
       }
     }
     __syncthreads();
-    for (int k0 = sl; k0 < ns; k0 += SL * NB) {
-      float4 a[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int k = sl + j * SL;
+      const float w = (k < ns) ? s_w[k] : 0.f;
+      if (w != 0.f) {
+        o.x = fmaf(w, a[j].x, o.x);
+        o.y = fmaf(w, a[j].y, o.y);
+        o.z = fmaf(w, a[j].z, o.z);
+        o.w = fmaf(w, a[j].w, o.w);
+        L = fmaf(w, s_l[k], L);
+      }
+    }
+    // partitions beyond SL * NB per pass: the remaining loads of this lane
+    for (int k0 = sl + SL * NB; k0 < ns; k0 += SL * NB) {
+      float4 b4[NB];
       float w[NB];
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
         const int k = k0 + j * SL;
         w[j] = (k < ns) ? s_w[k] : 0.f;
-        // dead partitions' numerators are never read
-        a[j] = (w[j] != 0.f) ? *reinterpret_cast<const float4*>(acc + (int64_t)(s0 + k) * sstride * D)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        b4[j] = (w[j] != 0.f) ? *reinterpret_cast<const float4*>(acc + (int64_t)(s0 + k) * sstride * D)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
         const int k = k0 + j * SL;
         if (w[j] != 0.f) {
-          o.x = fmaf(w[j], a[j].x, o.x);
-          o.y = fmaf(w[j], a[j].y, o.y);
-          o.z = fmaf(w[j], a[j].z, o.z);
-          o.w = fmaf(w[j], a[j].w, o.w);
+          o.x = fmaf(w[j], b4[j].x, o.x);
+          o.y = fmaf(w[j], b4[j].y, o.y);
+          o.z = fmaf(w[j], b4[j].z, o.z);
+          o.w = fmaf(w[j], b4[j].w, o.w);
           L = fmaf(w[j], s_l[k], L);
         }
       }

@@ -73,11 +73,12 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 24;  // consecutive idle polls of the scheduler / issuer
 constexpr int kMaxStages = 4;
 constexpr int kSBuf = 4;            // S/P buffers in TMEM
-constexpr int kCmdRing = 8;         // scheduler -> MMA issuer command ring
+constexpr int kCmdRing = 16;        // scheduler -> MMA issuer command ring
+constexpr unsigned kPollSleepNs = 32;  // back-off of the scheduler's and issuer's polls
 
 template <int D>
 struct Cfg {
-  static constexpr int kKStages = (D == 256) ? 2 : 3;      // fp16 K operand stages
+  static constexpr int kKStages = (D == 256) ? 2 : 4;      // fp16 K operand stages (pairs of tiles)
   static constexpr int kVStages = (D == 256) ? 2 : 3;      // fp16 V operand stages
   static constexpr int kRaw = (D == 256) ? 2 : 4;          // raw E4M3 stages per stream
   static constexpr int kQBytes = kRows * D * 2;            // Q tile (fp16, swizzled)
@@ -95,6 +96,7 @@ struct Cfg {
   static constexpr uint32_t kColS = 0;      // kSBuf x 64 columns; P(i) overwrites S(i)
   static constexpr uint32_t kColO = 256;    // D columns
   static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages && kRaw <= kMaxStages, "ring sizes");
+  static_assert(kKStages % 2 == 0, "K stages hold pairs of tiles");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
@@ -156,6 +158,22 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
+// Both halves of P (hi rows at taddr_hi, lo rows at taddr_lo), one wait.
+__device__ __forceinline__ void st_16x128b_x8_pair(uint32_t taddr_hi, uint32_t taddr_lo, const uint32_t (&h)[16],
+                                                   const uint32_t (&l)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+      "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};\n\t"
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%1], "
+      "{%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr_hi),
+      "r"(taddr_lo), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]), "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]),
+      "r"(h[8]), "r"(h[9]), "r"(h[10]), "r"(h[11]), "r"(h[12]), "r"(h[13]), "r"(h[14]), "r"(h[15]), "r"(l[0]),
+      "r"(l[1]), "r"(l[2]), "r"(l[3]), "r"(l[4]), "r"(l[5]), "r"(l[6]), "r"(l[7]), "r"(l[8]), "r"(l[9]),
+      "r"(l[10]), "r"(l[11]), "r"(l[12]), "r"(l[13]), "r"(l[14]), "r"(l[15])
+      : "memory");
+}
+
 // Exact E4M3 -> fp16 for two bytes (hardware conversion): dec(b) itself;
 // |dec| <= 448 and the subnormal quantum 2^-9 are both exact in fp16.
 // Four E4M3 bytes (little-endian in w) -> two fp16 pairs (bytes 0,1 and 2,3).
@@ -174,13 +192,13 @@ __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
 
 // Decode one raw tile (kT rows of D E4M3 bytes) into a swizzled fp16 operand
 // tile with the kDecThreads threads of a stream: column block db = d/64 holds
-// kT rows of 128 bytes; the 16-byte chunk c of row t sits at chunk position
+// kT rows of 128 bytes, DBS bytes after the previous block; the 16-byte chunk c of row t sits at chunk position
 // c ^ (t % 8).  Thread lt always takes raw chunk c = lt % (D/16) of rows
 // lt / (D/16) + k * R (R = rows per pass of all threads), so every address
 // is a per-thread base plus a compile-time offset; all loads are issued
 // before the first conversion.  Rows whose bit in `valid` is clear were not
 // copied and become zeros.
-template <int D>
+template <int D, int DBS>
 __device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uint64_t valid, int lt) {
   constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
   constexpr int kR = kDecThreads / kChunks; // rows per pass
@@ -195,7 +213,7 @@ __device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uin
   const int first = swap ? h0 + 1 : h0;
   const int second = swap ? h0 : h0 + 1;
   const uint8_t* src = raw + t0 * D + c * 16;
-  uint8_t* dst = op + db * (kT * 128) + t0 * 128;
+  uint8_t* dst = op + db * DBS + t0 * 128;
   const bool full = valid == ~0ull;
   uint4 w[kPer];
 #pragma unroll
@@ -445,7 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       if (i >= n_stages) {
         if (!mbar_wait(&op_empty[st], ((i / n_stages) - 1) & 1, kWaitLimit)) ok = false;
       }
-      decode_tile<D>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
+      if (is_k) {
+        // K stages hold pairs of tiles interleaved per column block, so that
+        // two consecutive tiles form one 128-row operand of the pair's QK
+        uint8_t* op = op_base + (st / 2) * (2 * C::kOpBytes) + (st % 2) * (kT * 128);
+        decode_tile<D, 2 * kT * 128>(raw_base + slot * C::kRawBytes, op, valid[slot], lt);
+      } else {
+        decode_tile<D, kT * 128>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
+      }
       fence_proxy_async_smem();
       mbar_arrive(&op_full[st]);
       mbar_arrive(&raw_empty[slot]);
@@ -453,16 +478,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
-    // Issues, in order, the chains the scheduler publishes.  It never probes
+    // Issues, in order, the chains the scheduler publishes: (1 << 16 | j) is
+    // the PV of tile j, (2 << 16 | m) the QK of tiles 2m and 2m+1.  It never probes
     // an mbarrier (a probe by the issuing thread waits until its outstanding
     // UMMAs have drained); the command ring is read with plain shared-memory
     // acquire loads.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16_f32(64, kT, false, false);
+      const uint32_t idesc_qk2 = idesc_f16_f32(64, 2 * kT, false, false);
       const uint32_t sq = smem_u32(smem + C::kOffQ);
       const uint32_t idesc_pv = idesc_f16_f32(128, D, false, true);
       bool ok = true;
-      const uint32_t n_cmd = 2u * (uint32_t)n_tiles;
+      const uint32_t n_cmd = (uint32_t)n_tiles + (uint32_t)(n_tiles + 1) / 2u;
       for (uint32_t c = 0; c < n_cmd && ok; ++c) {
         uint32_t spins = 0;
         while (ld_acquire_u32(&mt.cmd_head) <= c) {
@@ -470,11 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
             ok = false;
             break;
           }
+          __nanosleep(kPollSleepNs);  // leave issue slots to the softmax warp beside it
         }
         if (!ok) break;
         const uint32_t cmd = mt.cmd[c % kCmdRing];
         tc_fence_after();
-        if (cmd >> 16) {
+        if ((cmd >> 16) == 1u) {
           // PV(j): O += P(j) . V(j)
           const int j = (int)(cmd & 0xFFFFu);
           const int st = j % C::kVStages;
@@ -488,60 +516,78 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
           mma_commit(&mt.pv_done[j % kSBuf]);
           mma_commit(&mt.v_empty[st]);
         } else {
-          // QK(i): S(i) = Q . K(i)^T
-          const int i = (int)cmd;
-          const uint32_t sk = smem_u32(smem + C::kOffK + (i % C::kKStages) * C::kOpBytes);
+          // QK of the tile pair (i0, i0+1): S = Q . [K(i0); K(i0+1)]^T, one
+          // N=128 chain (N=64 for a last single tile)
+          const int i0 = 2 * (int)(cmd & 0xFFFFu), i1 = i0 + 1;
+          const bool two = i1 < n_tiles;
+          const int st0 = i0 % C::kKStages;
+          const uint32_t sk = smem_u32(smem + C::kOffK + (st0 / 2) * (2 * C::kOpBytes));
+          const uint32_t idesc = two ? idesc_qk2 : idesc_qk;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t bd = smem_desc(sk + (kk / 4) * (kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
+            const uint64_t bd = smem_desc(sk + (kk / 4) * (2 * kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
             const uint64_t ad = smem_desc(sq + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-            mma_ss(tmem + C::kColS + (i % kSBuf) * kT, ad, bd, idesc_qk, kk > 0);
+            mma_ss(tmem + C::kColS + (i0 % kSBuf) * kT, ad, bd, idesc, kk > 0);
           }
-          mma_commit(&mt.s_full[i % kSBuf]);
-          mma_commit(&mt.k_empty[i % C::kKStages]);
+          mma_commit(&mt.s_full[i0 % kSBuf]);
+          mma_commit(&mt.k_empty[st0]);
+          if (two) {
+            mma_commit(&mt.s_full[i1 % kSBuf]);
+            mma_commit(&mt.k_empty[st0 + 1]);
+          }
         }
-        st_release_u32(&mt.cmd_tail, c + 1);
+        // only the ring's free space depends on this counter: a relaxed store
+        // (a release store would wait for the UMMAs just issued)
+        st_relaxed_u32(&mt.cmd_tail, c + 1);
       }
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == kSchedWarp) {
     // ======================================================== scheduler
-    // Step i holds two independent chains: the QK of tile i and the PV of
-    // tile i-1.  Whichever is ready first is published first, so a PV never
-    // waits behind the decode of the next K tile, nor a QK behind a V tile
-    // still being decoded or a softmax still running.
+    // Two kinds of chains: the QK of a pair of tiles (both K tiles decoded,
+    // and the PVs of the tiles whose S/P buffers it overwrites done) and the
+    // PV of one tile (its P written and its V tile decoded).  A ready PV is
+    // published first, so the chain QK -> softmax -> PV of a tile never
+    // waits behind a QK that is ready early.
     if (lane == 0) {
       bool ok = true;
       uint32_t head = 0, spins = 0;
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        const int j = i - 1;
-        bool qk_todo = i < n_tiles, pv_todo = i >= 1;
-        while ((qk_todo || pv_todo) && ok) {
-          uint32_t cmd = 0;
-          bool have = false;
-          if (head - ld_acquire_u32(&mt.cmd_tail) < (uint32_t)kCmdRing) {
-            if (pv_todo && mbar_test(&mt.p_ready[j % kSBuf], (j / kSBuf) & 1) &&
-                mbar_test(&mt.v_full[j % C::kVStages], (j / C::kVStages) & 1)) {
-              cmd = (1u << 16) | (uint32_t)j;
-              pv_todo = false;
-              have = true;
-            } else if (qk_todo && mbar_test(&mt.k_full[i % C::kKStages], (i / C::kKStages) & 1) &&
-                       // S(i) overwrites the buffer that held P(i-4): PV(i-4) must be done
-                       (i < kSBuf || mbar_test(&mt.pv_done[i % kSBuf], ((i / kSBuf) - 1) & 1))) {
-              cmd = (uint32_t)i;
-              qk_todo = false;
+      const int n_pairs = (n_tiles + 1) / 2;
+      int qm = 0, pj = 0;  // next QK pair, next PV tile
+      auto done4 = [&](int t) {  // PV(t - 4) done, for the buffer tile t reuses
+        return t < kSBuf || mbar_test(&mt.pv_done[t % kSBuf], ((t / kSBuf) - 1) & 1);
+      };
+      while (pj < n_tiles && ok) {
+        uint32_t cmd = 0;
+        bool have = false;
+        if (head - ld_acquire_u32(&mt.cmd_tail) < (uint32_t)kCmdRing) {
+          if (pj < 2 * qm && mbar_test(&mt.p_ready[pj % kSBuf], (pj / kSBuf) & 1) &&
+              mbar_test(&mt.v_full[pj % C::kVStages], (pj / C::kVStages) & 1)) {
+            cmd = (1u << 16) | (uint32_t)pj;
+            ++pj;
+            have = true;
+          } else if (qm < n_pairs) {
+            const int i0 = 2 * qm, i1 = i0 + 1;
+            const bool two = i1 < n_tiles;
+            if (mbar_test(&mt.k_full[i0 % C::kKStages], (i0 / C::kKStages) & 1) &&
+                (!two || mbar_test(&mt.k_full[i1 % C::kKStages], (i1 / C::kKStages) & 1)) && done4(i0) &&
+                (!two || done4(i1))) {
+              cmd = (2u << 16) | (uint32_t)qm;
+              ++qm;
               have = true;
             }
           }
-          if (have) {
-            mt.cmd[head % kCmdRing] = cmd;
-            st_release_u32(&mt.cmd_head, head + 1);
-            ++head;
-            spins = 0;
-          } else if (++spins > kSpinLimit) {
-            ok = false;
-          }
+        }
+        if (have) {
+          mt.cmd[head % kCmdRing] = cmd;
+          st_release_u32(&mt.cmd_head, head + 1);
+          ++head;
+          spins = 0;
+        } else if (++spins > kSpinLimit) {
+          ok = false;
+        } else {
+          __nanosleep(kPollSleepNs);
         }
       }
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
@@ -605,14 +651,27 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
             }
           }
         }
+        // a tile every column of which both rows see takes the path
+        // without per-element selects (warp-uniform)
+        const bool full = __all_sync(0xffffffffu, vis == 0xFFFFFFFFu);
         float mx_a = -INFINITY, mx_b = -INFINITY;
+        if (full) {
 #pragma unroll
-        for (int gq = 0; gq < 8; ++gq)
+          for (int gq = 0; gq < 8; ++gq)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            if ((vis >> (2 * gq + e)) & 1u) mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * gq + e]) * c);
-            if ((vis >> (16 + 2 * gq + e)) & 1u) mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * gq + 2 + e]) * c);
-          }
+            for (int e = 0; e < 2; ++e) {
+              mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * gq + e]) * c);
+              mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * gq + 2 + e]) * c);
+            }
+        } else {
+#pragma unroll
+          for (int gq = 0; gq < 8; ++gq)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              if ((vis >> (2 * gq + e)) & 1u) mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * gq + e]) * c);
+              if ((vis >> (16 + 2 * gq + e)) & 1u) mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * gq + 2 + e]) * c);
+            }
+        }
         mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
         mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
@@ -630,17 +689,20 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         const float mu_b = (m_b == -INFINITY) ? 0.f : m_b;
         uint32_t ph[16], pl[16];
         float sum_a = 0.f, sum_b = 0.f;
+        // masked tokens get exactly 0 by selection (never 0 * x arithmetic)
+        const uint32_t vsel = full ? 0xFFFFFFFFu : vis;
 #pragma unroll
         for (int q2 = 0; q2 < 8; ++q2) {
-          // masked tokens get exactly 0 by selection (never 0 * x arithmetic)
-          const float pa0 =
-              ((vis >> (2 * q2)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2]), c, -mu_a)) : 0.f;
-          const float pa1 =
-              ((vis >> (2 * q2 + 1)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 1]), c, -mu_a)) : 0.f;
-          const float pb0 =
-              ((vis >> (16 + 2 * q2)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 2]), c, -mu_b)) : 0.f;
-          const float pb1 =
-              ((vis >> (17 + 2 * q2)) & 1u) ? fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 3]), c, -mu_b)) : 0.f;
+          float pa0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2]), c, -mu_a));
+          float pa1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 1]), c, -mu_a));
+          float pb0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 2]), c, -mu_b));
+          float pb1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 3]), c, -mu_b));
+          if (!full) {
+            pa0 = ((vsel >> (2 * q2)) & 1u) ? pa0 : 0.f;
+            pa1 = ((vsel >> (2 * q2 + 1)) & 1u) ? pa1 : 0.f;
+            pb0 = ((vsel >> (16 + 2 * q2)) & 1u) ? pb0 : 0.f;
+            pb1 = ((vsel >> (17 + 2 * q2)) & 1u) ? pb1 : 0.f;
+          }
           sum_a += pa0 + pa1;
           sum_b += pb0 + pb1;
           const uint32_t ha = pack_f16x2(pa0, pa1), hb = pack_f16x2(pb0, pb1);
@@ -680,9 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         }
         // P(i) replaces S(i) in its buffer: hi in lanes 32w+0..15, lo 16 above
         const uint32_t pcol = tmem + C::kColS + (i % kSBuf) * kT + lane_off;
-        st_16x128b_x8(pcol, ph);
-        st_16x128b_x8(pcol + (16u << 16), pl);
-        tmem_st_wait();
+        st_16x128b_x8_pair(pcol, pcol + (16u << 16), ph, pl);
       }
       tc_fence_before();
       // (one barrier per buffer: a warp without query vectors may already
