@@ -76,7 +76,7 @@ int generic_smem_bytes(int D, int row_chunk);
 
 // Tensor-core path: shared-memory bytes (D = 128 or 256), threads, tile size.
 int tc_smem_bytes(int D);
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 480;
 constexpr int kTcTileTokens = 64;
 constexpr int kTcRows = 64;
 constexpr int kTcMaxPartTiles = 32;  // longest partition of the tensor-core path (tiles)

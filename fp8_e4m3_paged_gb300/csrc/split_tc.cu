@@ -16,22 +16,32 @@
 //                zeros).  K and V have separate rings and producers because
 //                different MMAs free them: a K tile is free once its QK is
 //                done, a V tile only once its PV is;
-//   warp 12      TMEM allocation and UMMA issue (one elected thread);
+//   warp 12      TMEM allocation and UMMA issue (one thread), in a fixed
+//                order: the QK of pair m+1, then the PVs of pair m.  The
+//                thread waits on the mbarriers itself; every chain depends
+//                only on chains issued before it, so the order cannot
+//                deadlock, and the next pair's S is ready while the softmax
+//                still works on the current pair;
 //   warps 0-3    softmax: read S from TMEM, online softmax with FP32 state,
 //                write P = P_hi + P_lo (two fp16 halves) back to TMEM in place
-//                of S, rescale O when the running max jumps, epilogue.
-// Per 64-token tile:
-//   QK:  S[64 x 64] = Q[64 x D] . K^T   (UMMA M=64: A = Q resident in
-//        shared memory, B = K tile from shared memory, both K-major).  Query
-//        vector 16w+j (j < 16) lands in TMEM lane 32w+j.
-//   PV:  O[128 x D] += P[128 x 64] . V[64 x D]  (M=128, A from TMEM, B = V
-//        tile MN-major).  P_hi of vector 16w+j sits in lane 32w+j and its
+//                of S, rescale O (and the pair partner's P) when the running
+//                max jumps, epilogue.
+// Per pair of 64-token tiles (2m, 2m+1):
+//   QK:  S[64 x 128] = Q[64 x D] . [K(2m); K(2m+1)]^T  (one UMMA chain, M=64,
+//        N=128: A = Q resident in shared memory, B = the pair's K tiles,
+//        interleaved per column block, both K-major; N=64 for a last single
+//        tile).  Query vector 16w+j (j < 16) lands in TMEM lane 32w+j.
+//   PV:  O[128 x D] += P[128 x 64] . V[64 x D] per tile (M=128, A from TMEM,
+//        B = V tile MN-major), both tiles of the pair issued together once
+//        both P are written.  P_hi of vector 16w+j sits in lane 32w+j and its
 //        P_lo twin in lane 32w+16+j, so one MMA accumulates both halves of
 //        the probability split; the epilogue adds the two accumulator rows.
+// Barriers are per pair: the rings hold pairs of tiles and the QK, P and PV
+// of a pair complete together.
 // TMEM: four S/P buffers of 64 columns (P(i) overwrites S(i) in buffer i%4,
 // hi in the lanes the M=64 QK writes, lo in the 16 lanes above) and O.  With
-// four buffers the QK of tile i+4 is the first to wait for the PV of tile i,
-// so QK, softmax and PV of neighbouring tiles overlap.
+// four buffers the QK of pair m+2 is the first to wait for the PVs of pair
+// m, so QK, softmax and PV of neighbouring pairs overlap.
 // The hi/lo split keeps probabilities to ~22 bits ("compensated
 // probabilities"); the FP32 partition numerator, max and sum follow the FP32
 // state contract ("DFlash2 E4M3 attention with FP32 state", intro paragraph
@@ -65,21 +75,17 @@ constexpr int kKDecWarp0 = kSoftmaxWarps;              // 4
 constexpr int kVDecWarp0 = kKDecWarp0 + kDecWarps;     // 8
 constexpr int kMmaWarp = kVDecWarp0 + kDecWarps;       // 12
 constexpr int kProdWarp = kMmaWarp + 1;                // 13 (K), 14 (V)
-constexpr int kSchedWarp = kProdWarp + 2;              // 15
-constexpr int kThreads = 32 * (kSchedWarp + 1);        // 512
+constexpr int kThreads = 32 * (kProdWarp + 2);        // 480
 static_assert(kThreads == kTcThreads && kT == kTcTileTokens, "launch shape");
 constexpr float kTau = 8.0f;        // lazy-rescale threshold (base-2 units)
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kSpinLimit = 1u << 24;  // consecutive idle polls of the scheduler / issuer
 constexpr int kMaxStages = 4;
 constexpr int kSBuf = 4;            // S/P buffers in TMEM
-constexpr int kCmdRing = 16;        // scheduler -> MMA issuer command ring
-constexpr unsigned kPollSleepNs = 32;  // back-off of the scheduler's and issuer's polls
 
 template <int D>
 struct Cfg {
   static constexpr int kKStages = (D == 256) ? 2 : 4;      // fp16 K operand stages (pairs of tiles)
-  static constexpr int kVStages = (D == 256) ? 2 : 3;      // fp16 V operand stages
+  static constexpr int kVStages = (D == 256) ? 2 : 4;      // fp16 V operand stages (pairs of tiles)
   static constexpr int kRaw = (D == 256) ? 2 : 4;          // raw E4M3 stages per stream
   static constexpr int kQBytes = kRows * D * 2;            // Q tile (fp16, swizzled)
   static constexpr int kOpBytes = kT * D * 2;              // one K or V operand tile (fp16)
@@ -96,21 +102,21 @@ struct Cfg {
   static constexpr uint32_t kColS = 0;      // kSBuf x 64 columns; P(i) overwrites S(i)
   static constexpr uint32_t kColO = 256;    // D columns
   static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages && kRaw <= kMaxStages, "ring sizes");
-  static_assert(kKStages % 2 == 0, "K stages hold pairs of tiles");
+  static_assert(kKStages % 2 == 0 && kVStages % 2 == 0, "rings hold pairs of tiles");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
 struct Meta {
-  uint64_t k_full[kMaxStages], k_empty[kMaxStages];
-  uint64_t v_full[kMaxStages], v_empty[kMaxStages];
+  // operand rings, one barrier pair per two stages (a pair of tiles)
+  uint64_t k_full[kMaxStages / 2], k_empty[kMaxStages / 2];
+  uint64_t v_full[kMaxStages / 2], v_empty[kMaxStages / 2];
   uint64_t rawk_full[kMaxStages], rawv_full[kMaxStages];
   uint64_t rawk_empty[kMaxStages], rawv_empty[kMaxStages];
-  uint64_t s_full[kSBuf];               // per S/P buffer
-  uint64_t pv_done[kSBuf];
-  uint64_t p_ready[kSBuf];              // per buffer: a warp can run tiles ahead
+  // per pair of S/P buffers (tiles 2m, 2m+1 use buffers 2(m%2), 2(m%2)+1)
+  uint64_t s_full[2];                   // the pair's QK done
+  uint64_t p_ready[2];                  // both tiles' P written
+  uint64_t pv_done[2];                  // the pair's PVs done
   uint32_t tmem;
-  uint32_t cmd_head, cmd_tail;          // commands published / issued
-  uint32_t cmd[kCmdRing];               // (1 << 16 | tile): PV, tile: QK
   uint64_t validk[kMaxStages];          // per raw K stage: tokens that were copied
   uint64_t validv[kMaxStages];          // the same for the raw V stage
   uint32_t pmask[2][kE];                // sparse: entry masks of the tile each stream copies
@@ -137,18 +143,6 @@ __device__ __forceinline__ void ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32])
       : "r"(taddr));
 }
 
-// 16 lanes x 128 bits (4 columns) per repeat; thread t holds, per repeat g,
-// lane (t/4) column 4g + t%4, then lane (t/4 + 8) column 4g + t%4.
-__device__ __forceinline__ void st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -158,7 +152,40 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
+// Scale one half of a P tile in place: 16 lanes x 32 columns of f16x2 in the
+// 16x128b layout (thread t holds, per repeat g, lane t/4 column 4g + t%4 in
+// register 2g, then lane t/4 + 8 in register 2g+1); the rows of lane t/4 are
+// multiplied by al_a, those of lane t/4 + 8 by al_b.  Both factors are powers
+// of two, so the products are exact down to the fp16 subnormal range.
+__device__ __forceinline__ void scale_p_half(uint32_t taddr, float al_a, float al_b) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x128b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float al = (j & 1) ? al_b : al_a;
+    __half2 v = *reinterpret_cast<const __half2*>(&r[j]);
+    const float2 f = __half22float2(v);
+    v = __floats2half2_rn(f.x * al, f.y * al);
+    r[j] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 // Both halves of P (hi rows at taddr_hi, lo rows at taddr_lo), one wait.
+// 16 lanes x 128 bits (4 columns) per repeat; thread t holds, per repeat g,
+// lane (t/4) column 4g + t%4, then lane (t/4 + 8) column 4g + t%4.
 __device__ __forceinline__ void st_16x128b_x8_pair(uint32_t taddr_hi, uint32_t taddr_lo, const uint32_t (&h)[16],
                                                    const uint32_t (&l)[16]) {
   asm volatile(
@@ -304,15 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   // ---------------------------------------------------------- range
   int U;
   if (MODE == FP8KV_MODE_DENSE) {
-    U = 0;
-    for (int r = 0; r < p.q_max; ++r) {
-      int n = p.row_len[(int64_t)b * p.q_max + r];
-      if (n < 0 || n > p.max_kv_len) {
-        if (tid == 0) set_status(p.status, FP8KV_STATUS_BAD_LEN);
-        n = min(max(n, 0), p.max_kv_len);
-      }
-      U = max(U, n);
+    // the request's longest row: each warp loads the row lengths in
+    // parallel (one per lane) and reduces them
+    int n = 0;
+    bool bad = false;
+    for (int r = lane; r < p.q_max; r += 32) {
+      const int v = p.row_len[(int64_t)b * p.q_max + r];
+      bad |= (v < 0 || v > p.max_kv_len);
+      n = max(n, min(max(v, 0), p.max_kv_len));
     }
+    U = __reduce_max_sync(0xffffffffu, n);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (tid == 0 && any_bad) set_status(p.status, FP8KV_STATUS_BAD_LEN);
   } else {
     U = p.n_entries[b];
     if (U < 0 || U > p.max_blocks) {
@@ -334,12 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 
   // ---------------------------------------------------------- setup
   if (tid == 0) {
-    for (int i = 0; i < C::kKStages; ++i) {
-      mbar_init(&mt.k_full[i], kDecThreads);
+    for (int i = 0; i < C::kKStages / 2; ++i) {
+      mbar_init(&mt.k_full[i], 2 * kDecThreads);
       mbar_init(&mt.k_empty[i], 1);
     }
-    for (int i = 0; i < C::kVStages; ++i) {
-      mbar_init(&mt.v_full[i], kDecThreads);
+    for (int i = 0; i < C::kVStages / 2; ++i) {
+      mbar_init(&mt.v_full[i], 2 * kDecThreads);
       mbar_init(&mt.v_empty[i], 1);
     }
     for (int i = 0; i < C::kRaw; ++i) {
@@ -348,13 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       mbar_init(&mt.rawk_empty[i], kDecThreads);
       mbar_init(&mt.rawv_empty[i], kDecThreads);
     }
-    for (int i = 0; i < kSBuf; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&mt.s_full[i], 1);
       mbar_init(&mt.pv_done[i], 1);
-      mbar_init(&mt.p_ready[i], 32 * kSoftmaxWarps);
+      mbar_init(&mt.p_ready[i], 2 * 32 * kSoftmaxWarps);
     }
-    mt.cmd_head = 0;
-    mt.cmd_tail = 0;
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -458,10 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       const int slot = i % C::kRaw;
       const int st = i % n_stages;
       // raw rows arrived, and the operand stage is free (the MMA that read
-      // its previous tile is done)
+      // its previous tile, and that tile's partner, is done)
       if (!mbar_wait(&raw_full[slot], (i / C::kRaw) & 1, kWaitLimit)) ok = false;
       if (i >= n_stages) {
-        if (!mbar_wait(&op_empty[st], ((i / n_stages) - 1) & 1, kWaitLimit)) ok = false;
+        if (!mbar_wait(&op_empty[st / 2], ((i / n_stages) - 1) & 1, kWaitLimit)) ok = false;
       }
       if (is_k) {
         // K stages hold pairs of tiles interleaved per column block, so that
@@ -472,123 +500,69 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         decode_tile<D, kT * 128>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&op_full[st]);
+      mbar_arrive(&op_full[st / 2]);
+      if ((i & 1) == 0 && i + 1 == n_tiles) mbar_arrive(&op_full[st / 2]);  // a last tile without partner
       mbar_arrive(&raw_empty[slot]);
     }
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
-    // Issues, in order, the chains the scheduler publishes: (1 << 16 | j) is
-    // the PV of tile j, (2 << 16 | m) the QK of tiles 2m and 2m+1.  It never probes
-    // an mbarrier (a probe by the issuing thread waits until its outstanding
-    // UMMAs have drained); the command ring is read with plain shared-memory
-    // acquire loads.
+    // One thread issues every chain in a fixed order: QK(0), then for each
+    // pair m the QK of pair m+1 followed by the PVs of pair m.  Each chain
+    // waits only for work issued before it (K decoded, the PVs of the pair
+    // whose S/P buffers it reuses; P written, V decoded), so the order cannot
+    // deadlock, and the QK of the next pair is in flight while the softmax
+    // still works on the current one.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16_f32(64, kT, false, false);
       const uint32_t idesc_qk2 = idesc_f16_f32(64, 2 * kT, false, false);
       const uint32_t sq = smem_u32(smem + C::kOffQ);
       const uint32_t idesc_pv = idesc_f16_f32(128, D, false, true);
+      const int n_pairs = (n_tiles + 1) / 2;
       bool ok = true;
-      const uint32_t n_cmd = (uint32_t)n_tiles + (uint32_t)(n_tiles + 1) / 2u;
-      for (uint32_t c = 0; c < n_cmd && ok; ++c) {
-        uint32_t spins = 0;
-        while (ld_acquire_u32(&mt.cmd_head) <= c) {
-          if (++spins > kSpinLimit) {
-            ok = false;
-            break;
-          }
-          __nanosleep(kPollSleepNs);  // leave issue slots to the softmax warp beside it
-        }
-        if (!ok) break;
-        const uint32_t cmd = mt.cmd[c % kCmdRing];
+      // QK of the tile pair (2m, 2m+1): S = Q . [K(2m); K(2m+1)]^T, one
+      // N=128 chain (N=64 for a last single tile)
+      auto issue_qk = [&](int m) {
+        const int i0 = 2 * m;
+        const bool two = i0 + 1 < n_tiles;
+        const int st0 = i0 % C::kKStages;
+        if (!mbar_wait(&mt.k_full[st0 / 2], (i0 / C::kKStages) & 1, kWaitLimit)) ok = false;
+        if (m >= 2 && !mbar_wait(&mt.pv_done[m & 1], ((m >> 1) - 1) & 1, kWaitLimit)) ok = false;
         tc_fence_after();
-        if ((cmd >> 16) == 1u) {
-          // PV(j): O += P(j) . V(j)
-          const int j = (int)(cmd & 0xFFFFu);
-          const int st = j % C::kVStages;
-          const uint32_t sv = smem_u32(smem + C::kOffV + st * C::kOpBytes);
+        const uint32_t sk = smem_u32(smem + C::kOffK + (st0 / 2) * (2 * C::kOpBytes));
+        const uint32_t idesc = two ? idesc_qk2 : idesc_qk;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bd = smem_desc(sk + (kk / 4) * (2 * kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
+          const uint64_t ad = smem_desc(sq + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSw128);
+          mma_ss(tmem + C::kColS + (i0 % kSBuf) * kT, ad, bd, idesc, kk > 0);
+        }
+        mma_commit(&mt.s_full[m & 1]);
+        mma_commit(&mt.k_empty[st0 / 2]);
+      };
+      // PVs of the pair: O += P(2m) . V(2m) [+ P(2m+1) . V(2m+1)]
+      auto issue_pv = [&](int m) {
+        const int j0 = 2 * m;
+        const int sv0 = j0 % C::kVStages;
+        if (!mbar_wait(&mt.p_ready[m & 1], (m >> 1) & 1, kWaitLimit)) ok = false;
+        if (!mbar_wait(&mt.v_full[sv0 / 2], (j0 / C::kVStages) & 1, kWaitLimit)) ok = false;
+        tc_fence_after();
+        for (int j = j0; j < j0 + 2 && j < n_tiles; ++j) {
+          const uint32_t sv = smem_u32(smem + C::kOffV + (j % C::kVStages) * C::kOpBytes);
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk) {
             const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
             mma_ts(tmem + C::kColO, tmem + C::kColS + (j % kSBuf) * kT + kk * 8, bd, idesc_pv,
                    (j > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&mt.pv_done[j % kSBuf]);
-          mma_commit(&mt.v_empty[st]);
-        } else {
-          // QK of the tile pair (i0, i0+1): S = Q . [K(i0); K(i0+1)]^T, one
-          // N=128 chain (N=64 for a last single tile)
-          const int i0 = 2 * (int)(cmd & 0xFFFFu), i1 = i0 + 1;
-          const bool two = i1 < n_tiles;
-          const int st0 = i0 % C::kKStages;
-          const uint32_t sk = smem_u32(smem + C::kOffK + (st0 / 2) * (2 * C::kOpBytes));
-          const uint32_t idesc = two ? idesc_qk2 : idesc_qk;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t bd = smem_desc(sk + (kk / 4) * (2 * kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-            const uint64_t ad = smem_desc(sq + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-            mma_ss(tmem + C::kColS + (i0 % kSBuf) * kT, ad, bd, idesc, kk > 0);
-          }
-          mma_commit(&mt.s_full[i0 % kSBuf]);
-          mma_commit(&mt.k_empty[st0]);
-          if (two) {
-            mma_commit(&mt.s_full[i1 % kSBuf]);
-            mma_commit(&mt.k_empty[st0 + 1]);
-          }
         }
-        // only the ring's free space depends on this counter: a relaxed store
-        // (a release store would wait for the UMMAs just issued)
-        st_relaxed_u32(&mt.cmd_tail, c + 1);
-      }
-      if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp == kSchedWarp) {
-    // ======================================================== scheduler
-    // Two kinds of chains: the QK of a pair of tiles (both K tiles decoded,
-    // and the PVs of the tiles whose S/P buffers it overwrites done) and the
-    // PV of one tile (its P written and its V tile decoded).  A ready PV is
-    // published first, so the chain QK -> softmax -> PV of a tile never
-    // waits behind a QK that is ready early.
-    if (lane == 0) {
-      bool ok = true;
-      uint32_t head = 0, spins = 0;
-      const int n_pairs = (n_tiles + 1) / 2;
-      int qm = 0, pj = 0;  // next QK pair, next PV tile
-      auto done4 = [&](int t) {  // PV(t - 4) done, for the buffer tile t reuses
-        return t < kSBuf || mbar_test(&mt.pv_done[t % kSBuf], ((t / kSBuf) - 1) & 1);
+        mma_commit(&mt.pv_done[m & 1]);
+        mma_commit(&mt.v_empty[sv0 / 2]);
       };
-      while (pj < n_tiles && ok) {
-        uint32_t cmd = 0;
-        bool have = false;
-        if (head - ld_acquire_u32(&mt.cmd_tail) < (uint32_t)kCmdRing) {
-          if (pj < 2 * qm && mbar_test(&mt.p_ready[pj % kSBuf], (pj / kSBuf) & 1) &&
-              mbar_test(&mt.v_full[pj % C::kVStages], (pj / C::kVStages) & 1)) {
-            cmd = (1u << 16) | (uint32_t)pj;
-            ++pj;
-            have = true;
-          } else if (qm < n_pairs) {
-            const int i0 = 2 * qm, i1 = i0 + 1;
-            const bool two = i1 < n_tiles;
-            if (mbar_test(&mt.k_full[i0 % C::kKStages], (i0 / C::kKStages) & 1) &&
-                (!two || mbar_test(&mt.k_full[i1 % C::kKStages], (i1 / C::kKStages) & 1)) && done4(i0) &&
-                (!two || done4(i1))) {
-              cmd = (2u << 16) | (uint32_t)qm;
-              ++qm;
-              have = true;
-            }
-          }
-        }
-        if (have) {
-          mt.cmd[head % kCmdRing] = cmd;
-          st_release_u32(&mt.cmd_head, head + 1);
-          ++head;
-          spins = 0;
-        } else if (++spins > kSpinLimit) {
-          ok = false;
-        } else {
-          __nanosleep(kPollSleepNs);
-        }
+      issue_qk(0);
+      for (int m = 0; m < n_pairs && ok; ++m) {
+        if (m + 1 < n_pairs) issue_qk(m + 1);
+        if (ok) issue_pv(m);
       }
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     }
@@ -606,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     const int n_a = mt.nrow[ra], n_b = mt.nrow[rb];
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      if (!mbar_wait(&mt.s_full[i % kSBuf], (i / kSBuf) & 1, kWaitLimit)) ok = false;
+      if (!mbar_wait(&mt.s_full[(i >> 1) & 1], (i >> 2) & 1, kWaitLimit)) ok = false;
       tc_fence_after();
       if (warp_live) {
         uint32_t sr[32];
@@ -720,24 +694,36 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         l_b = l_b * alpha_b + sum_b;
 
         if (__any_sync(0xffffffffu, resc_a || resc_b)) {
-          // O must hold every earlier tile before it is rescaled: wait PV(i-1)
-          if (!mbar_wait(&mt.pv_done[(i - 1) % kSBuf], ((i - 1) / kSBuf) & 1, kWaitLimit)) ok = false;
-          tc_fence_after();
-          // thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16 (the
-          // P_hi row for lane < 16, its P_lo twin above); the alpha of vector
-          // 16w + x lives in thread 4*(x%8), as its a (x < 8) or b value.
-          const int x = lane & 15;
-          const float al_a = __shfl_sync(0xffffffffu, alpha_a, 4 * (x & 7));
-          const float al_b = __shfl_sync(0xffffffffu, alpha_b, 4 * (x & 7));
-          const float al = (x < 8) ? al_a : al_b;
+          // PVs run per pair of tiles: O holds the pairs before this tile's
+          // pair once their PVs are done, and for an odd tile the partner's P,
+          // made under the previous max, has not gone through its PV yet.
+          const int m = i >> 1;
+          if (m >= 1) {
+            if (!mbar_wait(&mt.pv_done[(m - 1) & 1], ((m - 1) >> 1) & 1, kWaitLimit)) ok = false;
+            tc_fence_after();
+            // thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16 (the
+            // P_hi row for lane < 16, its P_lo twin above); the alpha of vector
+            // 16w + x lives in thread 4*(x%8), as its a (x < 8) or b value.
+            const int x = lane & 15;
+            const float al_a = __shfl_sync(0xffffffffu, alpha_a, 4 * (x & 7));
+            const float al_b = __shfl_sync(0xffffffffu, alpha_b, 4 * (x & 7));
+            const float al = (x < 8) ? al_a : al_b;
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t o[16];
-            tmem_ld16(tmem + C::kColO + lane_off + c0, o);
-            tmem_ld_wait();
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t o[16];
+              tmem_ld16(tmem + C::kColO + lane_off + c0, o);
+              tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
-            tmem_st16(tmem + C::kColO + lane_off + c0, o);
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
+              tmem_st16(tmem + C::kColO + lane_off + c0, o);
+            }
+          }
+          if (i & 1) {
+            // P(i-1) *= alpha in place, hi and lo halves (rows ra, rb of
+            // this thread in both)
+            const uint32_t pc = tmem + C::kColS + ((i - 1) % kSBuf) * kT + lane_off;
+            scale_p_half(pc, alpha_a, alpha_b);
+            scale_p_half(pc + (16u << 16), alpha_a, alpha_b);
           }
         }
         // P(i) replaces S(i) in its buffer: hi in lanes 32w+0..15, lo 16 above
@@ -745,31 +731,37 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         st_16x128b_x8_pair(pcol, pcol + (16u << 16), ph, pl);
       }
       tc_fence_before();
-      // (one barrier per buffer: a warp without query vectors may already
-      // be on the next tile while another still writes this one's P)
-      mbar_arrive(&mt.p_ready[i % kSBuf]);
+      // one barrier per pair of buffers (a warp without query vectors may
+      // already be on the next pair while another still writes this one)
+      mbar_arrive(&mt.p_ready[(i >> 1) & 1]);
+      if ((i & 1) == 0 && i + 1 == n_tiles) mbar_arrive(&mt.p_ready[(i >> 1) & 1]);  // last tile without partner
     }
     // ------------------------------------------------------ epilogue
-    if (!mbar_wait(&mt.pv_done[(n_tiles - 1) % kSBuf], ((n_tiles - 1) / kSBuf) & 1, kWaitLimit)) ok = false;
+    const int last_pair = (n_tiles - 1) >> 1;
+    if (!mbar_wait(&mt.pv_done[last_pair & 1], (last_pair >> 1) & 1, kWaitLimit)) ok = false;
     tc_fence_after();
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     if (warp_live) {
+      // O row of vector 16w + x: P_hi part in lane x, P_lo part in lane
+      // x + 16.  Per 64 columns the two lanes swap halves, so that lane x
+      // sums and stores columns 0..31 and lane x + 16 columns 32..63.
       const int myrow = 16 * warp + (lane & 15);
-      float* dst = p.partial + (prow + myrow) * D;
+      const bool up = lane >= 16;
+      float* dst = p.partial + (prow + myrow) * D + (up ? 32 : 0);
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t o[16];
-        tmem_ld16(tmem + C::kColO + lane_off + c0, o);
-        tmem_ld_wait();
-        float v[16];
+      for (int c0 = 0; c0 < D; c0 += 64) {
+        uint32_t o[64];
+        tmem_ld64(tmem + C::kColO + lane_off + c0, o);
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float xo = __uint_as_float(o[j]);
-          v[j] = xo + __shfl_down_sync(0xffffffffu, xo, 16);
+        for (int j = 0; j < 32; ++j) {
+          const float keep = __uint_as_float(up ? o[j + 32] : o[j]);
+          const float give = __uint_as_float(up ? o[j] : o[j + 32]);
+          v[j] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
         }
-        if (lane < 16 && myrow < RC) {
+        if (myrow < RC) {
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
+          for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
       }
