@@ -328,6 +328,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   const int row0 = chunk * p.row_chunk;
   const int RC = min(p.row_chunk, p.rows - row0);
 
+  // ---------------------------------------------------------- loads
+  // Everything the setup reads from global memory is requested up front,
+  // so its latencies overlap: this thread's share of the Q tile, the live
+  // length (or query row) of query vector tid, and the row lengths that
+  // fix the partition range.
+  constexpr int kQChunks = kRows * (D / 8);                     // 16-byte Q chunks
+  constexpr int kQPer = (kQChunks + kThreads - 1) / kThreads;
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int idx = tid + k * kThreads;
+    const int i = idx / (D / 8), c8 = idx % (D / 8);  // row, 8-element chunk
+    qv[k] = make_uint4(0, 0, 0, 0);
+    if (idx < kQChunks && i < RC) {
+      const int rowi = row0 + i;
+      const int r = rowi / p.G, h = g * p.G + rowi % p.G;
+      qv[k] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D + c8 * 8);
+    }
+  }
+  int my_nrow = -1;
+  if (tid < RC) {
+    const int r = (row0 + tid) / p.G;
+    my_nrow = (MODE == FP8KV_MODE_DENSE) ? min(max(p.row_len[(int64_t)b * p.q_max + r], 0), p.max_kv_len) : r;
+  }
+
   // ---------------------------------------------------------- range
   int U;
   if (MODE == FP8KV_MODE_DENSE) {
@@ -389,36 +414,24 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     tmem_alloc(&mt.tmem, C::kTmemCols);
     tmem_relinquish();
   }
-  for (int i = tid; i < kRows; i += kThreads) {
-    int n = -1;
-    if (i < RC) {
-      const int r = (row0 + i) / p.G;
-      n = (MODE == FP8KV_MODE_DENSE) ? min(max(p.row_len[(int64_t)b * p.q_max + r], 0), p.max_kv_len) : r;
-    }
-    mt.nrow[i] = n;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = mt.tmem;
-
+  static_assert(kRows <= kThreads, "one query vector per thread");
+  if (tid < kRows) mt.nrow[tid] = my_nrow;
   // Q rows -> swizzled K-major tile in shared memory (rows >= RC are zero)
   uint8_t* sQ = smem + C::kOffQ;
-  for (int idx = tid; idx < kRows * (D / 8); idx += kThreads) {
-    const int i = idx / (D / 8), c8 = idx % (D / 8);  // row, 8-element chunk
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (i < RC) {
-      const int rowi = row0 + i;
-      const int r = rowi / p.G, h = g * p.G + rowi % p.G;
-      v = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D + c8 * 8);
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int idx = tid + k * kThreads;
+    if (idx < kQChunks) {
+      const int i = idx / (D / 8), c8 = idx % (D / 8);
+      const int db = c8 / 8, ch = c8 % 8;
+      *reinterpret_cast<uint4*>(sQ + db * (kRows * 128) + i * 128 + ((ch ^ (i & 7)) * 16)) = qv[k];
     }
-    const int db = c8 / 8, ch = c8 % 8;
-    *reinterpret_cast<uint4*>(sQ + db * (kRows * 128) + i * 128 + ((ch ^ (i & 7)) * 16)) = v;
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const uint32_t tmem = mt.tmem;
 
   if (warp == kProdWarp || warp == kProdWarp + 1) {
     // ======================================================== producers
