@@ -8,7 +8,9 @@ Inputs stay resident in HBM; several copies of the KV pool are rotated so
 that each step reads bytes the L2 no longer holds.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle
-instead, on bounded samples of the same workload.
+instead, on bounded samples of the same workload.  ``--op cache_write``
+measures the cache write instead (a 65536-token prefill chunk of fp16 K/V,
+Hkv=8, D=128, quantised into 16-token E4M3 pages).
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
 torchrun, each rank runs an independent replica (no collective on the data
@@ -32,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from synth import attended_kv_bytes, make_problem  # noqa: E402
+from synth import attended_kv_bytes, make_cache_write, make_problem  # noqa: E402
 
 METRIC = "attended-KV GB/s and µs/step (q8 Hq6/Hkv1/D256 @128K ctx), % of HBM peak"
 WORKLOAD_DESC = {
@@ -440,6 +442,196 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+CW_METRIC = "cache-write GB/s (fp16 K/V -> E4M3 pages: 65536 tokens, Hkv=8, D=128, page 16), % of HBM peak"
+CW_DESC = ("prefill chunk of 65536 new tokens (5% padding slots), Hkv=8, D=128, fp16 K and V with "
+           "per-tensor scales 0.0071 / 0.0123, written into 16-token E4M3 pages of a 4608-block pool in "
+           "allocator order")
+
+
+def _cw_problem():
+    # scales as an amax calibration gives them (not powers of two)
+    return make_cache_write(N=65536, Hkv=8, D=128, page_size=16, num_blocks=4608, seed=5, bad_slots=0,
+                            k_scale=0.0071, v_scale=0.0123)
+
+
+def _cw_bytes(p):
+    """Algorithmic bytes of one write: the slot list, and per written token
+    the fp16 K and V rows read and the E4M3 K and V rows written."""
+    N, Hkv, D = p.k.shape
+    live = int(((p.slots >= 0) & (p.slots < p.num_blocks * p.page_size)).sum())
+    return N * 8 + live * Hkv * D * (2 + 2 + 1 + 1), live
+
+
+def run_cache_write(args):
+    from fp8_e4m3_paged_gb300 import binding as B
+    from fp8_e4m3_paged_gb300 import build_lib
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    build_lib.build()
+    p = _cw_problem()
+    bytes_step, live = _cw_bytes(p)
+    dev = torch.device("cuda")
+    k, v, slots = p.k.to(dev), p.v.to(dev), p.slots.to(dev)
+    kc0, vc0 = p.empty_caches()
+    kc, vc = kc0.to(dev), vc0.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = B.make_cache_write_args(k=k, v=v, slot_mapping=slots, k_cache=kc, v_cache=vc, page_size=p.page_size,
+                                k_scale=p.k_scale, v_scale=p.v_scale, status=status)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.fp8kv_attn_cache_write(a, s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.fp8kv_attn_cache_write(a, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    steps = args.steps
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):  # inputs (268 MB) and output (134 MB) exceed the L2
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    ms = e0.elapsed_time(e1) / steps
+    # e2e: the same write through the C ABI with the step's inputs copied
+    # from pinned host memory and the status word read back
+    host = {"k": p.k.pin_memory(), "v": p.v.pin_memory(), "s": p.slots.pin_memory()}
+    devs = {"k": k, "v": v, "s": slots}
+    st_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.e2e_steps, steps))
+
+    def e2e_step():
+        for key, t in host.items():
+            devs[key].copy_(t, non_blocking=True)
+        B.fp8kv_attn_cache_write(a, torch.cuda.current_stream().cuda_stream)
+        st_h.copy_(status, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    peak, peak_src = _peaks()
+    value = bytes_step / (ms * 1e-3) / 1e9
+    line = {
+        "op": "cache_write",
+        "metric": CW_METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": 1,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 6),
+        "us_per_step": round(ms * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; N(0,1) fp16 rows with saturating outliers)",
+        "config": {"workload": f"cache_write: {CW_DESC}", "written_tokens": live,
+                   "l2": "inputs larger than L2: 268 MB read and 134 MB written per step",
+                   "launch": "one CUDA graph per step, replayed back to back"},
+        "roofline": {"bound": "hbm", "kernel": "cache_write", "achieved": round(value, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_step, "avg_launch_us": round(ms * 1e3, 3),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "clocks": sampler.summary(t0, t1),
+        "e2e": {"value": round(bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": steps,
+        "device_status": int(status.item()),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cw_cpu_baseline(p, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def _cw_sample(p, lo, n):
+    sub = make_cache_write(N=0, Hkv=p.k.shape[1], D=p.k.shape[2], page_size=p.page_size,
+                           num_blocks=p.num_blocks)
+    sub.k, sub.v, sub.slots = p.k[lo:lo + n], p.v[lo:lo + n], p.slots[lo:lo + n]
+    sub.k_scale, sub.v_scale = p.k_scale, p.v_scale
+    return sub
+
+
+def cw_cpu_baseline(p, budget_s):
+    """The oracle's cache write (single thread) on consecutive slices of the
+    workload until the budget is spent; bytes counted like the GPU's."""
+    import oracle
+
+    oracle.build()
+    kc, vc = p.empty_caches()
+    n, lo, done, t0 = 256, 0, 0, time.time()
+    while time.time() - t0 < budget_s:
+        sub = _cw_sample(p, lo, n)
+        oracle.cache_write(sub.k, sub.v, sub.slots, kc, vc, sub.k_scale, sub.v_scale, sub.page_size)
+        done += _cw_bytes(sub)[0]
+        lo = (lo + n) % p.k.shape[0]
+    dt = time.time() - t0
+    return {"value": round(done / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 2), "sample": "consecutive 256-token slices of the workload, one thread"}
+
+
+def run_cache_write_reference(args):
+    _, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    p = _cw_problem()
+    kc, vc = p.empty_caches()
+    n = 64
+    per = args.ref_budget / max(1, args.steps + args.warmup)
+    probe = _cw_sample(p, 0, n)
+    t = time.time()
+    oracle.cache_write(probe.k, probe.v, probe.slots, kc, vc, p.k_scale, p.v_scale, p.page_size)
+    n = int(max(16, min(p.k.shape[0], n * per / max(time.time() - t, 1e-4))))
+    for _ in range(args.warmup):
+        sub = _cw_sample(p, 0, n)
+        oracle.cache_write(sub.k, sub.v, sub.slots, kc, vc, p.k_scale, p.v_scale, p.page_size)
+    done, t0 = 0, time.time()
+    for i in range(args.steps):
+        sub = _cw_sample(p, (i * n) % p.k.shape[0], n)
+        oracle.cache_write(sub.k, sub.v, sub.slots, kc, vc, p.k_scale, p.v_scale, p.page_size)
+        done += _cw_bytes(sub)[0]
+    dt = time.time() - t0
+    value = done / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "op": "cache_write", "metric": CW_METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; N(0,1) fp16 rows with saturating outliers)",
+        "config": {"workload": f"cache_write: {CW_DESC}"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} consecutive tokens per step, bytes counted like the GPU's"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,10 +644,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["attention", "cache_write"], default="attention")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.op == "cache_write":
+        if args.impl == "reference":
+            run_cache_write_reference(args)
+        else:
+            run_cache_write(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -75,6 +75,29 @@ class Args(ctypes.Structure):
     ]
 
 
+DTYPE_F16 = 0
+DTYPE_BF16 = 1
+
+
+class CacheWriteArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("num_kv_blocks", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("k_stride_token", ctypes.c_int64), ("k_stride_head", ctypes.c_int64),
+        ("v_stride_token", ctypes.c_int64), ("v_stride_head", ctypes.c_int64),
+        ("slot_mapping", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("kc_stride_block", ctypes.c_int64), ("kc_stride_token", ctypes.c_int64),
+        ("kc_stride_head", ctypes.c_int64),
+        ("vc_stride_block", ctypes.c_int64), ("vc_stride_token", ctypes.c_int64),
+        ("vc_stride_head", ctypes.c_int64),
+        ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+        ("k_scale_dev", ctypes.c_void_p), ("v_scale_dev", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build it with `python -m fp8_e4m3_paged_gb300.build_lib` "
@@ -92,6 +115,10 @@ STATIC_SCRATCH_BYTES = 16 << 20
 for _n in ("fp8kv_attn_split", "fp8kv_attn_combine", "fp8kv_attn_forward_static"):
     getattr(lib, _n).restype = ctypes.c_int
     getattr(lib, _n).argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), ctypes.c_void_p]
+
+
+lib.fp8kv_attn_cache_write.restype = ctypes.c_int
+lib.fp8kv_attn_cache_write.argtypes = [ctypes.POINTER(CacheWriteArgs), ctypes.c_void_p]
 
 
 class Fp8kvError(RuntimeError):
@@ -204,3 +231,38 @@ class Call:
     def run(self, stream: int) -> None:
         self.split(stream)
         self.combine(stream)
+
+
+def fp8kv_attn_cache_write(args: CacheWriteArgs, stream: int = 0) -> None:
+    rc = lib.fp8kv_attn_cache_write(ctypes.byref(args), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_cache_write")
+
+
+def make_cache_write_args(*, k, v, slot_mapping, k_cache, v_cache, page_size: int,
+                          k_scale: float = 1.0, v_scale: float = 1.0, k_scale_dev=None,
+                          v_scale_dev=None, status=None) -> CacheWriteArgs:
+    """Fill a CacheWriteArgs struct from torch CUDA tensors.
+
+    k / v: float16 or bfloat16 [N][Hkv][D] (d contiguous); slot_mapping:
+    int64 [N]; k_cache / v_cache: uint8 [blocks][page_size][Hkv][D] views
+    (d contiguous); status: optional int32 tensor of one element."""
+    import torch
+
+    a = CacheWriteArgs()
+    N, Hkv, D = k.shape
+    a.num_tokens, a.num_kv_heads, a.head_dim = N, Hkv, D
+    a.page_size = page_size
+    a.num_kv_blocks = k_cache.shape[0]
+    a.dtype = DTYPE_F16 if k.dtype == torch.float16 else DTYPE_BF16
+    a.k, a.v = _ptr(k), _ptr(v)
+    a.k_stride_token, a.k_stride_head = k.stride(0), k.stride(1)
+    a.v_stride_token, a.v_stride_head = v.stride(0), v.stride(1)
+    a.slot_mapping = _ptr(slot_mapping)
+    a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
+    a.kc_stride_block, a.kc_stride_token, a.kc_stride_head = k_cache.stride()[:3]
+    a.vc_stride_block, a.vc_stride_token, a.vc_stride_head = v_cache.stride()[:3]
+    a.k_scale, a.v_scale = float(k_scale), float(v_scale)
+    a.k_scale_dev, a.v_scale_dev = _ptr(k_scale_dev), _ptr(v_scale_dev)
+    a.status = _ptr(status)
+    return a

@@ -235,3 +235,26 @@ extern "C" int fp8kv_attn_combine(const fp8kv_attn_plan_t* plan, const fp8kv_att
   const cudaError_t e = launch_combine(plan, p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
 }
+
+extern "C" int fp8kv_attn_cache_write(const fp8kv_cache_write_args* a, fp8kv_stream_t stream) {
+  if (!a) return FP8KV_EINVAL;
+  if (a->num_tokens < 0 || a->num_kv_heads < 1 || a->page_size < 1 || a->num_kv_blocks < 1)
+    return FP8KV_EINVAL;
+  if (a->head_dim < 16 || a->head_dim > 1024 || (a->head_dim % 16) != 0) return FP8KV_EINVAL;
+  if (a->dtype != FP8KV_DTYPE_F16 && a->dtype != FP8KV_DTYPE_BF16) return FP8KV_EINVAL;
+  if (a->num_tokens == 0) return FP8KV_OK;
+  if (!a->k || !a->v || !a->slot_mapping || !a->k_cache || !a->v_cache) return FP8KV_EINVAL;
+  if (!aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16))
+    return FP8KV_EINVAL;
+  const int64_t es[4] = {a->k_stride_token, a->k_stride_head, a->v_stride_token, a->v_stride_head};
+  for (int64_t s : es)
+    if (s < 0 || (s % 8) != 0) return FP8KV_EINVAL;
+  const int64_t bs[6] = {a->kc_stride_block, a->kc_stride_token, a->kc_stride_head,
+                         a->vc_stride_block, a->vc_stride_token, a->vc_stride_head};
+  for (int64_t s : bs)
+    if (s < 0 || (s % 16) != 0) return FP8KV_EINVAL;
+  if (!a->k_scale_dev && !(std::isfinite(a->k_scale) && a->k_scale > 0.f)) return FP8KV_EINVAL;
+  if (!a->v_scale_dev && !(std::isfinite(a->v_scale) && a->v_scale > 0.f)) return FP8KV_EINVAL;
+  const cudaError_t e = launch_cache_write(*a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}

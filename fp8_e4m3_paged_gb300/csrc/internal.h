@@ -54,6 +54,7 @@ int build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params
 cudaError_t launch_split_generic(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
+cudaError_t launch_cache_write(const fp8kv_cache_write_args& a, cudaStream_t s);
 
 // Runs a setup call (a kernel attribute) once per device, on first use.
 struct DeviceOnce {

@@ -185,6 +185,57 @@ int fp8kv_attn_split(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
 int fp8kv_attn_combine(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
                        fp8kv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Cache write: quantise new K/V rows into the E4M3 pages.
+ *
+ * For every new token n < num_tokens with slot = slot_mapping[n] >= 0, block
+ * slot / page_size, offset slot % page_size, and every KV head h, d < D:
+ *
+ *   k_cache[block][offset][h][d] = E4M3(fp32(k[n][h][d]) / k_scale)
+ *   v_cache[block][offset][h][d] = E4M3(fp32(v[n][h][d]) / v_scale)
+ *
+ * with the division in FP32 (correctly rounded) and E4M3() rounding to the
+ * nearest code, ties to even, magnitudes above 448 saturating to +-448 and
+ * NaN giving a NaN code.  This is the write path that fills the cache the
+ * attention reads, with the layer's per-tensor scales ("Qwen4Exp: fp8_e4m3
+ * main KV cache on the QSA path", PR description: the uint8 cache is written
+ * with the per-tensor scales and read back as e4m3).  Slots < 0 (padding
+ * tokens) are not written; a slot whose block is outside [0, num_kv_blocks)
+ * is not written either and sets FP8KV_STATUS_BAD_BLOCK in *status when
+ * status is not NULL.  Two tokens that name the same slot race (last writer
+ * unspecified), as in any scatter.
+ * ------------------------------------------------------------------------ */
+#define FP8KV_DTYPE_F16 0
+#define FP8KV_DTYPE_BF16 1
+
+typedef struct {
+  int32_t num_tokens;     /* N >= 0 new tokens (0: nothing to do) */
+  int32_t num_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;       /* D: a multiple of 16, 16..1024 */
+  int32_t page_size;      /* tokens per physical block, >= 1 */
+  int32_t num_kv_blocks;  /* physical blocks in the pool, >= 1 */
+  int32_t dtype;          /* FP8KV_DTYPE_F16 or FP8KV_DTYPE_BF16 (k and v) */
+  const void* k;          /* 2-byte elements; (n, h, d) at element n*k_stride_token + h*k_stride_head + d */
+  const void* v;          /* same with the v_stride_* values */
+  int64_t k_stride_token, k_stride_head;  /* elements, multiples of 8 (16-byte rows), >= 0 */
+  int64_t v_stride_token, v_stride_head;
+  const int64_t* slot_mapping;            /* [N] block * page_size + offset; < 0 = skip */
+  uint8_t* k_cache;       /* same addressing as fp8kv_attn_args.k_cache */
+  uint8_t* v_cache;
+  int64_t kc_stride_block, kc_stride_token, kc_stride_head; /* bytes, multiples of 16 */
+  int64_t vc_stride_block, vc_stride_token, vc_stride_head; /* bytes, multiples of 16 */
+  float k_scale;          /* host K scale, > 0 (used when k_scale_dev is NULL) */
+  float v_scale;          /* host V scale, > 0 (used when v_scale_dev is NULL) */
+  const float* k_scale_dev; /* optional device scalar, NULL = host */
+  const float* v_scale_dev;
+  uint32_t* status;       /* optional device word for FP8KV_STATUS_BAD_BLOCK, NULL = none */
+} fp8kv_cache_write_args;
+
+/* Launch the cache write on `stream`.  k, v and the caches must be 16-byte
+ * aligned.  Returns FP8KV_EINVAL for bad arguments, FP8KV_ECUDA if the launch
+ * fails; never allocates or synchronises (graph-capturable). */
+int fp8kv_attn_cache_write(const fp8kv_cache_write_args* a, fp8kv_stream_t stream);
+
 /* Size of the library-owned device scratch used by fp8kv_attn_forward_static
  * (16 MiB; one copy per GPU that loads the library, held until exit). */
 #define FP8KV_STATIC_SCRATCH_BYTES (16u << 20)

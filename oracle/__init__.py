@@ -9,6 +9,12 @@ it with ctypes.  Inputs are ``synth.Problem`` objects (CPU tensors).
 
 Parity status of each exported function (what pins it, in ``tests/``):
   e4m3 table          format definition closed form + torch float8_e4m3fn
+  e4m3 encode         round trip of every code, exact midpoints (ties to
+                      even), nearest on both sides of each midpoint,
+                      saturation, signed zero, torch float8_e4m3fn in range
+  cache write         slot placement, skipped and out-of-range slots,
+                      strides, decode(write(x)) within half a quantum of
+                      x / scale, power-of-two scales against the encoder
   fp16 decode         all 65536 codes against numpy float16
   attention           exact-rational evaluation on tiny inputs, closed forms
                       (single token, constant keys, two tokens), invariants
@@ -92,6 +98,14 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.orc_attention_split.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_abs.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
     lib.orc_row_weights.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.orc_bf16.restype = ctypes.c_double
+    lib.orc_bf16.argtypes = [ctypes.c_uint16]
+    vp = ctypes.c_void_p
+    lib.orc_cache_write.restype = ctypes.c_int
+    lib.orc_cache_write.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float,
+                                                         vp, vp, vp, vp]
     _libs[plant] = lib
     return lib
 
@@ -206,3 +220,40 @@ def row_weights(p, b: int, r: int, h: int, plant: int = 0, **over) -> np.ndarray
     buf = np.zeros(cap, dtype=np.float64)
     n = load(plant).orc_row_weights(ctypes.byref(pin.s), b, r, h, buf.ctypes.data, cap)
     return buf[:n].copy()
+
+
+def e4m3_encode(y, plant: int = 0) -> np.ndarray:
+    """E4M3 bytes of float32 values (round to nearest even, saturating)."""
+    lib = load(plant)
+    a = np.asarray(y, dtype=np.float32).reshape(-1)
+    return np.array([lib.orc_e4m3_encode(float(x)) for x in a], dtype=np.uint8).reshape(np.shape(y))
+
+
+def bf16_value(bits: int, plant: int = 0) -> float:
+    return load(plant).orc_bf16(bits)
+
+
+def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: float,
+                page_size: int, plant: int = 0) -> int:
+    """Write new tokens into E4M3 cache tensors in place (CPU).
+
+    k, v: float16 or bfloat16 [N][Hkv][D] (any strides, d contiguous);
+    slot_mapping: int64 [N] (slot = block * page_size + offset, < 0 = skip);
+    k_cache, v_cache: uint8 [blocks][page_size][Hkv][D] views (any strides,
+    d contiguous), modified in place.  Returns the number of slots whose
+    block lies outside the cache (skipped)."""
+    assert k.dtype == v.dtype and k.dtype in (torch.float16, torch.bfloat16)
+    for t in (k, v, k_cache, v_cache):
+        assert t.device.type == "cpu" and t.stride(-1) == 1
+    N, Hkv, D = k.shape
+    dtype = 0 if k.dtype == torch.float16 else 1
+    kb, vb = k.view(torch.int16), v.view(torch.int16)
+    sm = slot_mapping.to(torch.int64).contiguous()
+    kes = np.array(kb.stride()[:2], dtype=np.int64)
+    ves = np.array(vb.stride()[:2], dtype=np.int64)
+    kbs = np.array(k_cache.stride()[:3], dtype=np.int64)
+    vbs = np.array(v_cache.stride()[:3], dtype=np.int64)
+    return load(plant).orc_cache_write(
+        N, Hkv, D, page_size, k_cache.shape[0], dtype, kb.data_ptr(), vb.data_ptr(),
+        kes.ctypes.data, ves.ctypes.data, sm.data_ptr(), float(k_scale), float(v_scale),
+        k_cache.data_ptr(), v_cache.data_ptr(), kbs.ctypes.data, vbs.ctypes.data)

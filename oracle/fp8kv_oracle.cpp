@@ -115,6 +115,89 @@ ORC_API double orc_f16(uint16_t h) {
   return s ? -v : v;
 }
 
+// ---------------------------------------------------------------- encoder
+
+// Value -> E4M3 byte: the nearest representable value, ties to the code with
+// an even mantissa (round to nearest, ties to even), magnitudes beyond the
+// largest finite value 448 saturate to it (infinities included), the sign of
+// zero and of values that round to zero is kept, NaN gives 0x7F.  The
+// nearest value is found by comparing against all 127 finite magnitudes
+// (exact in double: every candidate has at most 4 significant bits and the
+// input has 24).  This is the cache write's rounding ("Qwen4Exp: fp8_e4m3
+// main KV cache on the QSA path", PR description: the cache is written with
+// the layer's per-tensor scales, round to nearest even with saturation to
+// the finite range being the plain reading of an E4M3FN store).
+ORC_API uint8_t orc_e4m3_encode(float y) {
+  if (std::isnan(y)) return 0x7F;
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  if (std::isinf(y)) return (uint8_t)(sign | 0x7E);
+  const double a = std::fabs((double)y);
+  int best = 0;
+  double best_d = std::numeric_limits<double>::infinity();
+  for (int c = 0; c < 0x7F; ++c) {  // magnitudes in increasing order, 0x7F is NaN
+    const double d = std::fabs(a - orc_e4m3((uint8_t)c));
+#if ORC_PLANT == 9
+    if (d < best_d || (d == best_d && c > best)) {  // planted: ties away from zero
+#else
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+#endif
+      best_d = d;
+      best = c;
+    }
+  }
+#if ORC_PLANT == 10
+  if (a > 448.0) return (uint8_t)(sign | 0x7F);  // planted: overflow to NaN instead of saturating
+#endif
+  return (uint8_t)(sign | best);
+}
+
+// bfloat16 bits -> value (the upper half of a binary32).
+ORC_API double orc_bf16(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+// Cache write: for every new token n with slot = slot_mapping[n] >= 0, block
+// slot / page_size, offset slot % page_size, and every KV head h and d < D:
+//   k_cache[block, offset, h, d] = encode(fp32(k[n][h][d]) / fp32(k_scale))
+// and the same for V (fp32 division, correctly rounded, then the encoder
+// above).  Inputs are binary16 (dtype 0) or bfloat16 (dtype 1) bit patterns
+// with element strides (token, head); caches use byte strides (block, token,
+// head).  Slots whose block is outside [0, num_blocks) are skipped and
+// counted in the return value.
+ORC_API int orc_cache_write(int N, int Hkv, int D, int page_size, int num_blocks, int dtype,
+                            const uint16_t* k, const uint16_t* v, const int64_t* k_es, const int64_t* v_es,
+                            const int64_t* slot_mapping, float k_scale, float v_scale,
+                            uint8_t* k_cache, uint8_t* v_cache, const int64_t* k_bs, const int64_t* v_bs) {
+  int bad = 0;
+  for (int n = 0; n < N; ++n) {
+    const int64_t slot = slot_mapping[n];
+    if (slot < 0) continue;
+    const int64_t blk = slot / page_size;
+#if ORC_PLANT == 11
+    const int64_t off = slot % page_size + 1;  // planted: slot offset off by one
+#else
+    const int64_t off = slot % page_size;
+#endif
+    if (blk >= num_blocks || off >= page_size) {
+      ++bad;
+      continue;
+    }
+    for (int h = 0; h < Hkv; ++h)
+      for (int d = 0; d < D; ++d) {
+        const uint16_t kb = k[n * k_es[0] + h * k_es[1] + d];
+        const uint16_t vb = v[n * v_es[0] + h * v_es[1] + d];
+        const float kx = (float)(dtype == 0 ? orc_f16(kb) : orc_bf16(kb));
+        const float vx = (float)(dtype == 0 ? orc_f16(vb) : orc_bf16(vb));
+        k_cache[blk * k_bs[0] + off * k_bs[1] + h * k_bs[2] + d] = orc_e4m3_encode(kx / k_scale);
+        v_cache[blk * v_bs[0] + off * v_bs[1] + h * v_bs[2] + d] = orc_e4m3_encode(vx / v_scale);
+      }
+  }
+  return bad;
+}
+
 // ------------------------------------------------------- visible token set
 
 struct Tok { int64_t k_off, v_off; };

@@ -1,9 +1,10 @@
 """Seeded synthetic inputs for FP8 E4M3 paged attention.
 
 This package only *makes data*: query vectors, E4M3 key/value page pools,
-block tables, per-row live lengths and QSA microblock tables with visibility
-masks.  It contains none of the attention arithmetic, and it is the only code
-shared by the CPU oracle (``oracle/``) and the CUDA library
+block tables, per-row live lengths, QSA microblock tables with visibility
+masks, and new fp16/bf16 K/V rows with their cache slots.  It contains none
+of the attention or quantisation arithmetic, and it is the only code shared
+by the CPU oracle (``oracle/``) and the CUDA library
 (``fp8_e4m3_paged_gb300``).
 """
 
@@ -16,3 +17,4 @@ from .workloads import (  # noqa: F401
     quantize_e4m3,
     attended_kv_bytes,
 )
+from .cache_write import CacheWriteProblem, make_cache_write  # noqa: F401

@@ -145,3 +145,36 @@ def test_batch0_launch_is_noop(B):
     a.workspace_bytes = plan.workspace_bytes
     assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == 0
     assert B.lib.fp8kv_attn_combine(ctypes.byref(plan), ctypes.byref(a), None) == 0
+
+
+# ------------------------------------------------------------------ cache write (host validation only)
+
+def _cw(B, **kw):
+    a = B.CacheWriteArgs()
+    a.num_tokens, a.num_kv_heads, a.head_dim, a.page_size, a.num_kv_blocks, a.dtype = 4, 2, 128, 16, 8, 0
+    # aligned but never dereferenced: every call below is rejected on the host
+    a.k = a.v = a.k_cache = a.v_cache = a.slot_mapping = 0x10000
+    a.k_stride_token, a.k_stride_head = 256, 128
+    a.v_stride_token, a.v_stride_head = 256, 128
+    a.kc_stride_block, a.kc_stride_token, a.kc_stride_head = 4096, 256, 128
+    a.vc_stride_block, a.vc_stride_token, a.vc_stride_head = 4096, 256, 128
+    a.k_scale = a.v_scale = 1.0
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(num_tokens=-1), dict(num_kv_heads=0), dict(head_dim=24), dict(head_dim=0), dict(head_dim=2048),
+    dict(page_size=0), dict(num_kv_blocks=0), dict(dtype=2), dict(k=0), dict(slot_mapping=0),
+    dict(v_cache=0), dict(k=0x10008), dict(k_stride_token=3), dict(v_stride_head=-8),
+    dict(kc_stride_token=8), dict(vc_stride_block=-16), dict(k_scale=0.0), dict(v_scale=float("nan")),
+])
+def test_cache_write_rejects_bad_arguments(B, bad):
+    assert B.lib.fp8kv_attn_cache_write(ctypes.byref(_cw(B, **bad)), None) == B.EINVAL
+
+
+def test_cache_write_empty_and_null(B):
+    assert B.lib.fp8kv_attn_cache_write(None, None) == B.EINVAL
+    # no tokens: nothing to launch, pointers may be null
+    assert B.lib.fp8kv_attn_cache_write(ctypes.byref(_cw(B, num_tokens=0, k=0, v=0)), None) == B.OK
