@@ -10,7 +10,8 @@ that each step reads bytes the L2 no longer holds.
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle
 instead, on bounded samples of the same workload.  ``--op cache_write``
 measures the cache write instead (a 65536-token prefill chunk of fp16 K/V,
-Hkv=8, D=128, quantised into 16-token E4M3 pages).
+Hkv=8, D=128, quantised into 16-token E4M3 pages), ``--op dcp_merge`` the
+context-parallel merge kernel on a decode batch.
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
 torchrun, each rank runs an independent replica (no collective on the data
@@ -632,6 +633,74 @@ def run_cache_write_reference(args):
     }), flush=True)
 
 
+DCP_METRIC = "DCP merge GB/s and µs (2048 query vectors, D=128, R ranks' FP32 outputs + base-2 LSEs -> fp16)"
+
+
+def run_dcp_merge(args):
+    """The cross-rank merge kernel (all-to-all shape's local merge) on a
+    decode batch: 64 requests x 32 query heads, D=128, for R = 2, 4, 8 ranks.
+    The value is R=2; enough input copies rotate that each merge reads bytes
+    the L2 no longer holds."""
+    from fp8_e4m3_paged_gb300 import binding as B
+    from fp8_e4m3_paged_gb300 import build_lib
+
+    _, _, local = _dist()
+    torch.cuda.set_device(local)
+    build_lib.build()
+    n, D = 64 * 32, 128
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    g = torch.Generator(device="cuda").manual_seed(3)
+    peak, peak_src = _peaks()
+    res = {}
+    for R in (2, 4, 8):
+        per = R * n * (D + 1) * 4
+        copies = max(2, math.ceil(3 * l2 / per))
+        outs = torch.randn(copies, R, n, D, device="cuda", generator=g)
+        lses = torch.randn(copies, R, n, device="cuda", generator=g) * 4
+        out = torch.empty(n, D, dtype=torch.float16, device="cuda")
+        argl = [B.make_merge_args(outs=outs[c], lses=lses[c], out=out) for c in range(copies)]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            B.fp8kv_attn_merge(argl[0], s.cuda_stream)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for c in range(copies):
+                B.fp8kv_attn_merge(argl[c], torch.cuda.current_stream().cuda_stream)
+        reps = max(3, args.steps // copies)
+        with torch.cuda.stream(s):
+            for _ in range(max(3, args.warmup // copies)):
+                gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+        alg = per + n * D * 2
+        res[R] = {"us": round(us, 3), "gbs": round(alg / (us * 1e-6) / 1e9, 2), "bytes": alg, "copies": copies,
+                  "launches": reps * copies}
+    line = {
+        "op": "dcp_merge", "metric": DCP_METRIC, "value": res[2]["gbs"], "unit": "GB/s", "n_gpus": 1,
+        "steps": res[2]["launches"], "warmup": args.warmup, "ms_per_step": round(res[2]["us"] / 1e3, 6),
+        "us_per_step": res[2]["us"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (N(0,1) outputs, N(0,16) LSEs)",
+        "config": {"workload": "dcp_merge: 64 decode requests x 32 query heads, D=128, R=2 "
+                               "(R=4 and 8 under per_rank_count)",
+                   "per_rank_count": res,
+                   "l2": "inputs larger than L2: rotating input copies"},
+        "roofline": {"bound": "hbm", "kernel": "merge", "achieved": res[2]["gbs"], "peak": peak, "unit": "GB/s",
+                     "frac": round(res[2]["gbs"] / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": res[2]["bytes"], "avg_launch_us": res[2]["us"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+        "gpu_launches": res[2]["launches"],
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -644,11 +713,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "cache_write"], default="attention")
+    ap.add_argument("--op", choices=["attention", "cache_write", "dcp_merge"], default="attention")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.op == "cache_write":
+    if args.op == "dcp_merge":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "dcp_merge",
+                              "unavailable": "the merge is timed on the GPU only; its oracle is pinned in tests"}))
+        else:
+            run_dcp_merge(args)
+    elif args.op == "cache_write":
         if args.impl == "reference":
             run_cache_write_reference(args)
         else:

@@ -98,6 +98,18 @@ class CacheWriteArgs(ctypes.Structure):
     ]
 
 
+MERGE_MAX_RANKS = 64
+
+
+class MergeArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_ranks", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("num_vectors", ctypes.c_int64),
+        ("outs", ctypes.c_void_p), ("rank_stride_out", ctypes.c_int64),
+        ("lses", ctypes.c_void_p), ("rank_stride_lse", ctypes.c_int64),
+        ("out", ctypes.c_void_p), ("out_f32", ctypes.c_void_p), ("lse_out", ctypes.c_void_p),
+    ]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build it with `python -m fp8_e4m3_paged_gb300.build_lib` "
@@ -117,6 +129,13 @@ for _n in ("fp8kv_attn_split", "fp8kv_attn_combine", "fp8kv_attn_forward_static"
     getattr(lib, _n).argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), ctypes.c_void_p]
 
 
+lib.fp8kv_attn_combine_lse.restype = ctypes.c_int
+lib.fp8kv_attn_combine_lse.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Args), ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]
+lib.fp8kv_attn_merge.restype = ctypes.c_int
+lib.fp8kv_attn_merge.argtypes = [ctypes.POINTER(MergeArgs), ctypes.c_void_p]
+lib.fp8kv_attn_merge_scale.restype = ctypes.c_int
+lib.fp8kv_attn_merge_scale.argtypes = [ctypes.POINTER(MergeArgs), ctypes.c_int32, ctypes.c_void_p]
 lib.fp8kv_attn_cache_write.restype = ctypes.c_int
 lib.fp8kv_attn_cache_write.argtypes = [ctypes.POINTER(CacheWriteArgs), ctypes.c_void_p]
 
@@ -266,3 +285,36 @@ def make_cache_write_args(*, k, v, slot_mapping, k_cache, v_cache, page_size: in
     a.k_scale_dev, a.v_scale_dev = _ptr(k_scale_dev), _ptr(v_scale_dev)
     a.status = _ptr(status)
     return a
+
+
+def fp8kv_attn_combine_lse(plan: Plan, args: Args, out_f32, lse, stream: int = 0) -> None:
+    """Combine one rank's shard into FP32 output [B][q][Hq][D] and base-2 LSE [B][q][Hq]."""
+    rc = lib.fp8kv_attn_combine_lse(ctypes.byref(plan), ctypes.byref(args), _ptr(out_f32), _ptr(lse),
+                                    ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_combine_lse")
+
+
+def make_merge_args(*, outs, lses, out=None, out_f32=None, lse_out=None) -> MergeArgs:
+    """outs: FP32 [R][n..][D]; lses: FP32 [R][n..] (torch CUDA tensors; the
+    vector dimensions are flattened, the rank dimension may be strided)."""
+    R, D = outs.shape[0], outs.shape[-1]
+    a = MergeArgs()
+    a.num_ranks, a.head_dim = R, D
+    a.num_vectors = lses[0].numel() if R > 0 else 0
+    a.outs, a.rank_stride_out = _ptr(outs), outs.stride(0)
+    a.lses, a.rank_stride_lse = _ptr(lses), lses.stride(0)
+    a.out, a.out_f32, a.lse_out = _ptr(out), _ptr(out_f32), _ptr(lse_out)
+    return a
+
+
+def fp8kv_attn_merge(args: MergeArgs, stream: int = 0) -> None:
+    rc = lib.fp8kv_attn_merge(ctypes.byref(args), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_merge")
+
+
+def fp8kv_attn_merge_scale(args: MergeArgs, rank: int, stream: int = 0) -> None:
+    rc = lib.fp8kv_attn_merge_scale(ctypes.byref(args), rank, ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_merge_scale")

@@ -137,7 +137,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   return FP8KV_OK;
 }
 
-int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params* p) {
+int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params* p, bool need_out) {
   if (!plan || !a || !p) return FP8KV_EINVAL;
   if (plan->revision != FP8KV_ATTN_REVISION) return FP8KV_EVERSION;
   std::memset(p, 0, sizeof(*p));
@@ -164,8 +164,9 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
     p->status = reinterpret_cast<unsigned int*>(a->workspace);
     return FP8KV_OK;
   }
-  if (!a->q || !a->out || !a->k_cache || !a->v_cache) return FP8KV_EINVAL;
-  if (!aligned(a->q, 16) || !aligned(a->out, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16))
+  if (!a->q || (need_out && !a->out) || !a->k_cache || !a->v_cache) return FP8KV_EINVAL;
+  if (!aligned(a->q, 16) || (need_out && !aligned(a->out, 16)) || !aligned(a->k_cache, 16) ||
+      !aligned(a->v_cache, 16))
     return FP8KV_EINVAL;
   const int64_t st[6] = {a->k_stride_block, a->k_stride_token, a->k_stride_head,
                          a->v_stride_block, a->v_stride_token, a->v_stride_head};
@@ -256,5 +257,50 @@ extern "C" int fp8kv_attn_cache_write(const fp8kv_cache_write_args* a, fp8kv_str
   if (!a->k_scale_dev && !(std::isfinite(a->k_scale) && a->k_scale > 0.f)) return FP8KV_EINVAL;
   if (!a->v_scale_dev && !(std::isfinite(a->v_scale) && a->v_scale > 0.f)) return FP8KV_EINVAL;
   const cudaError_t e = launch_cache_write(*a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}
+
+extern "C" int fp8kv_attn_combine_lse(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, float* out_f32,
+                                      float* lse, fp8kv_stream_t stream) {
+  Params p;
+  const int rc = build_params(plan, a, &p, false);
+  if (rc != FP8KV_OK) return rc;
+  if (p.B == 0) return FP8KV_OK;
+  if (!out_f32 || !lse || !aligned(out_f32, 16) || !aligned(lse, 4)) return FP8KV_EINVAL;
+  p.out_f32 = out_f32;
+  p.lse = lse;
+  const cudaError_t e = launch_combine(plan, p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}
+
+namespace {
+
+int check_merge(const fp8kv_merge_args* a) {
+  if (!a) return FP8KV_EINVAL;
+  if (a->num_ranks < 1 || a->num_ranks > FP8KV_MERGE_MAX_RANKS || a->num_vectors < 0) return FP8KV_EINVAL;
+  if (a->head_dim < 4 || a->head_dim > 1024 || (a->head_dim % 4) != 0) return FP8KV_EINVAL;
+  if (a->num_vectors == 0) return FP8KV_OK;
+  if (!a->outs || !aligned(a->outs, 16) || a->rank_stride_out < 0 || (a->rank_stride_out % 4) != 0)
+    return FP8KV_EINVAL;
+  if (!a->lses || a->rank_stride_lse < 0) return FP8KV_EINVAL;
+  if ((a->out && !aligned(a->out, 8)) || (a->out_f32 && !aligned(a->out_f32, 16))) return FP8KV_EINVAL;
+  return FP8KV_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8kv_attn_merge(const fp8kv_merge_args* a, fp8kv_stream_t stream) {
+  const int rc = check_merge(a);
+  if (rc != FP8KV_OK || a->num_vectors == 0) return rc;
+  if (!a->out && !a->out_f32 && !a->lse_out) return FP8KV_EINVAL;
+  const cudaError_t e = launch_merge(*a, -1, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}
+
+extern "C" int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, fp8kv_stream_t stream) {
+  const int rc = check_merge(a);
+  if (rc != FP8KV_OK || a->num_vectors == 0) return rc;
+  if (rank < 0 || rank >= a->num_ranks || !a->out_f32 || a->out || a->lse_out) return FP8KV_EINVAL;
+  const cudaError_t e = launch_merge(*a, rank, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
 }

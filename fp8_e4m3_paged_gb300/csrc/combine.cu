@@ -35,6 +35,12 @@ constexpr int MAXS = 1024;  // partitions whose weights are staged per pass
 constexpr int KR = MAXS / CT;  // (m, l) pairs a thread holds
 constexpr int NB = 12;      // numerator loads in flight per lane (S <= 192 in one trip)
 
+// LSE = false: fp16 output.  LSE = true: FP32 output and the vector's
+// base-2 log-sum-exp M + log2(L) (-inf when nothing is visible), the pair a
+// context-parallel rank hands to the cross-rank merge ("Qualify calibrated
+// E4M3 and disk PLE with QSA DCP2", commit exposing base-2 LSE and FP32
+// partial output).
+template <bool LSE>
 __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   __shared__ float red_m[CT / 32];
   __shared__ float s_w[MAXS];       // weight 2^(m_s - M) of live partitions (0 = dead)
@@ -60,6 +66,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   const float* acc = p.partial + base * D + slice * DW + c4 * 4;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
+  float M = -INFINITY;
   for (int s0 = 0; s0 < S; s0 += MAXS) {
     const int ns = min(MAXS, S - s0);
     // one trip to memory: the (m, l) pairs of this pass and, speculatively,
@@ -101,7 +108,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
       __syncthreads();  // the previous pass is done with s_w / s_l
     }
     __syncthreads();
-    float M = red_m[0];
+    M = red_m[0];
 #pragma unroll
     for (int k = 1; k < CT / 32; ++k) M = fmaxf(M, red_m[k]);
     if (M == -INFINITY) break;  // nothing visible for this vector
@@ -172,6 +179,11 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
     const float y1 = (Lt > 0.f) ? t.y * f : 0.f;
     const float y2 = (Lt > 0.f) ? t.z * f : 0.f;
     const float y3 = (Lt > 0.f) ? t.w * f : 0.f;
+    if (LSE) {
+      *reinterpret_cast<float4*>(p.out_f32 + (int64_t)idx * D + slice * DW + tid * 4) = make_float4(y0, y1, y2, y3);
+      if (slice == 0 && tid == 0) p.lse[idx] = (Lt > 0.f) ? M + log2f(Lt) : -INFINITY;
+      return;
+    }
     const __half2 h01 = __floats2half2_rn(y0, y1);
     const __half2 h23 = __floats2half2_rn(y2, y3);
     uint2 pk;
@@ -188,7 +200,10 @@ cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaS
   if (n == 0) return cudaSuccess;
   if (p.D % DW) return cudaErrorInvalidValue;
   (void)plan;
-  combine_kernel<<<(unsigned)n, CT, 0, st>>>(p);
+  if (p.out_f32)
+    combine_kernel<true><<<(unsigned)n, CT, 0, st>>>(p);
+  else
+    combine_kernel<false><<<(unsigned)n, CT, 0, st>>>(p);
   return cudaGetLastError();
 }
 

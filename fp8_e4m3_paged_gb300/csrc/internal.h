@@ -47,14 +47,17 @@ struct Params {
   unsigned int* status;
   float* partial;   // [B][Hkv][S][rows][D]
   float2* ml;       // [B][Hkv][S][rows]  (max in log2 units, sum)
+  float* out_f32;   // combine with LSE: FP32 output [B][q_max][Hq][D] (NULL: fp16 out)
+  float* lse;       // combine with LSE: base-2 LSE [B][q_max][Hq]
 };
 
-int build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params* p);
+int build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params* p, bool need_out = true);
 
 cudaError_t launch_split_generic(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_cache_write(const fp8kv_cache_write_args& a, cudaStream_t s);
+cudaError_t launch_merge(const fp8kv_merge_args& a, int32_t scale_rank, cudaStream_t s);
 
 // Runs a setup call (a kernel attribute) once per device, on first use.
 struct DeviceOnce {

@@ -236,6 +236,50 @@ typedef struct {
  * fails; never allocates or synchronises (graph-capturable). */
 int fp8kv_attn_cache_write(const fp8kv_cache_write_args* a, fp8kv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Context-parallel merge ("Qualify calibrated E4M3 and disk PLE with QSA
+ * DCP2": each rank holding a shard of the context exposes a base-2 LSE and
+ * an FP32 partial output, merged across ranks by an all-gather of the LSEs
+ * plus a reduce-scatter of the outputs, or by one all-to-all).
+ *
+ * fp8kv_attn_combine_lse is fp8kv_attn_combine for one rank's shard: instead
+ * of the fp16 output it writes, per query vector, the FP32 output o (v_scale
+ * applied) and lse = log2(sum_j 2^(log2(e) z_j)) over the shard's visible
+ * tokens (o = 0, lse = -inf when the shard shows the vector nothing).
+ * a->out is not used and may be NULL.
+ *
+ * fp8kv_attn_merge merges R ranks' (o_r, lse_r) pairs of n vectors:
+ *   L = log2(sum_r 2^lse_r),  out = sum_r 2^(lse_r - L) o_r
+ * (the attention over the union of the shards), writing any of: fp16 out
+ * (RNE), FP32 out_f32, lse_out = L.  Vectors that no rank sees get +0.0 and
+ * -inf.  The ranks are summed in order (bitwise deterministic).  With R = 1
+ * and lses all finite it converts an FP32 output to fp16.
+ *
+ * fp8kv_attn_merge_scale is the all-gather + reduce-scatter shape: `outs`
+ * holds this rank's own o (rank_stride_out unused), `lses` the all-gathered
+ * LSEs of all R ranks, and out_f32 receives 2^(lse_rank - L) o_rank; summing
+ * that over the ranks (the reduce-scatter) gives the merged FP32 output.
+ * ------------------------------------------------------------------------ */
+#define FP8KV_MERGE_MAX_RANKS 64
+
+typedef struct {
+  int32_t num_ranks;        /* R: 1..FP8KV_MERGE_MAX_RANKS */
+  int32_t head_dim;         /* D: multiple of 4, 4..1024 */
+  int64_t num_vectors;      /* n >= 0 (0: nothing to do) */
+  const float* outs;        /* rank r's vector i at outs + r*rank_stride_out + i*D (16-byte aligned) */
+  int64_t rank_stride_out;  /* elements, multiple of 4 */
+  const float* lses;        /* rank r's vector i at lses + r*rank_stride_lse + i */
+  int64_t rank_stride_lse;  /* elements */
+  void* out;                /* fp16 [n][D] or NULL (8-byte aligned) */
+  float* out_f32;           /* FP32 [n][D] or NULL (16-byte aligned) */
+  float* lse_out;           /* [n] or NULL */
+} fp8kv_merge_args;
+
+int fp8kv_attn_combine_lse(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, float* out_f32,
+                           float* lse, fp8kv_stream_t stream);
+int fp8kv_attn_merge(const fp8kv_merge_args* a, fp8kv_stream_t stream);
+int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, fp8kv_stream_t stream);
+
 /* Size of the library-owned device scratch used by fp8kv_attn_forward_static
  * (16 MiB; one copy per GPU that loads the library, held until exit). */
 #define FP8KV_STATIC_SCRATCH_BYTES (16u << 20)

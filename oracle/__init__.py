@@ -12,6 +12,11 @@ Parity status of each exported function (what pins it, in ``tests/``):
   e4m3 encode         round trip of every code, exact midpoints (ties to
                       even), nearest on both sides of each midpoint,
                       saturation, signed zero, torch float8_e4m3fn in range
+  attention_lse       merging the (out, lse) of disjoint context shards gives
+                      the full attention and its LSE; one-token and
+                      equal-logit closed forms of the LSE
+  merge               one rank is the identity, an empty rank changes
+                      nothing, shards of one problem merge to the whole
   cache write         slot placement, skipped and out-of-range slots,
                       strides, decode(write(x)) within half a quantum of
                       x / scale, power-of-two scales against the encoder
@@ -98,6 +103,10 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.orc_attention_split.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_abs.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
     lib.orc_row_weights.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_attention_lse.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_merge.restype = None
+    lib.orc_merge.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_void_p]
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
     lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
     lib.orc_bf16.restype = ctypes.c_double
@@ -257,3 +266,27 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: f
         N, Hkv, D, page_size, k_cache.shape[0], dtype, kb.data_ptr(), vb.data_ptr(),
         kes.ctypes.data, ves.ctypes.data, sm.data_ptr(), float(k_scale), float(v_scale),
         k_cache.data_ptr(), v_cache.data_ptr(), kbs.ctypes.data, vbs.ctypes.data)
+
+
+def attention_lse(p, threads: Optional[int] = None, plant: int = 0, **over):
+    """(out [B][q][Hq][D], lse [B][q][Hq]) in float64; lse is base 2."""
+    pin = _Pinned(p, **over)
+    out = np.zeros((p.B, p.q, p.Hq, p.D), dtype=np.float64)
+    lse = np.zeros((p.B, p.q, p.Hq), dtype=np.float64)
+    rc = load(plant).orc_attention_lse(ctypes.byref(pin.s), out.ctypes.data, lse.ctypes.data,
+                                       threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
+    return out, lse
+
+
+def merge(outs, lses, plant: int = 0):
+    """Merge R ranks' outputs [R][..][D] and base-2 LSEs [R][..]."""
+    o = np.ascontiguousarray(np.asarray(outs, dtype=np.float64))
+    l = np.ascontiguousarray(np.asarray(lses, dtype=np.float64))
+    R, D = o.shape[0], o.shape[-1]
+    n = int(np.prod(l.shape[1:]))
+    m = np.zeros(o.shape[1:], dtype=np.float64)
+    lm = np.zeros(l.shape[1:], dtype=np.float64)
+    load(plant).orc_merge(R, n, D, o.ctypes.data, l.ctypes.data, m.ctypes.data, lm.ctypes.data)
+    return m, lm

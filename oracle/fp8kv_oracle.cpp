@@ -452,5 +452,81 @@ ORC_API int orc_attention_split(const orc_problem* p, int num_splits, double* ou
   return 0;
 }
 
+// ---------------------------------------------------- context-parallel merge
+
+// Output and base-2 log-sum-exp of every query vector: out as orc_attention,
+// lse = log2(sum_j 2^(log2(e) z_j)) over the visible tokens (-inf for a dead
+// row).  A rank that holds a shard of the context emits this pair; merging
+// the ranks' pairs gives the attention over the union ("Qualify calibrated
+// E4M3 and disk PLE with QSA DCP2", commit exposing base-2 LSE and FP32
+// partial output for cross-rank merging).
+static void row_head_lse(const orc_problem* p, int b, int r, int h, double* out, double* lse) {
+  row_head(p, b, r, h, out);
+  std::vector<Tok> toks;
+  visible(p, b, r, group_of(p, h), toks);
+  if (toks.empty()) {
+    *lse = -std::numeric_limits<double>::infinity();
+    return;
+  }
+  std::vector<double> z;
+  logits(p, b, r, h, toks, z);
+  double M = -std::numeric_limits<double>::infinity();
+  for (double v : z) M = std::max(M, v);
+  double S = 0.0;
+  for (double v : z) S += std::exp(v - M);
+#if ORC_PLANT == 13
+  S = 1.0;  // planted: the sum dropped from the log-sum-exp
+#endif
+  *lse = (M + std::log(S)) / std::log(2.0);
+}
+
+ORC_API int orc_attention_lse(const orc_problem* p, double* out, double* lse, int nthreads) {
+  if (check(p)) return -1;
+  const int64_t n = (int64_t)p->B * p->q * p->Hq;
+  parallel_items(n, nthreads, [&](int64_t i) {
+    const int h = (int)(i % p->Hq);
+    const int r = (int)((i / p->Hq) % p->q);
+    const int b = (int)(i / ((int64_t)p->Hq * p->q));
+    row_head_lse(p, b, r, h, out + i * p->D, lse + i);
+  });
+  return 0;
+}
+
+// Merge R ranks' (out, lse) pairs of n vectors: L = log2(sum_r 2^lse_r),
+// merged = sum_r 2^(lse_r - L) out_r (the softmax over the union of the
+// shards, written per rank); a vector that no rank sees gets 0 and -inf.
+ORC_API void orc_merge(int R, int64_t n, int D, const double* out, const double* lse, double* merged,
+                       double* lse_merged) {
+  for (int64_t i = 0; i < n; ++i) {
+    double L = -std::numeric_limits<double>::infinity();
+    for (int r = 0; r < R; ++r) L = std::max(L, lse[(int64_t)r * n + i]);
+    double* m = merged + i * D;
+    for (int d = 0; d < D; ++d) m[d] = 0.0;
+    if (L == -std::numeric_limits<double>::infinity()) {
+      lse_merged[i] = L;
+      continue;
+    }
+    double W = 0.0;
+    for (int r = 0; r < R; ++r) {
+#if ORC_PLANT == 12
+      W += std::exp(lse[(int64_t)r * n + i] - L);  // planted: natural base for base-2 LSEs
+#else
+      W += std::exp2(lse[(int64_t)r * n + i] - L);
+#endif
+    }
+    for (int r = 0; r < R; ++r) {
+#if ORC_PLANT == 12
+      const double w = std::exp(lse[(int64_t)r * n + i] - L) / W;
+#else
+      const double w = std::exp2(lse[(int64_t)r * n + i] - L) / W;
+#endif
+      if (w == 0.0) continue;
+      const double* o = out + ((int64_t)r * n + i) * D;
+      for (int d = 0; d < D; ++d) m[d] += w * o[d];
+    }
+    lse_merged[i] = L + std::log2(W);
+  }
+}
+
 ORC_API int orc_abi_version(void) { return 1; }
 
