@@ -11,7 +11,8 @@ Prints ONE JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle
 instead, on bounded samples of the same workload.  ``--op cache_write``
 measures the cache write instead (a 65536-token prefill chunk of fp16 K/V,
 Hkv=8, D=128, quantised into 16-token E4M3 pages), ``--op dcp_merge`` the
-context-parallel merge kernel on a decode batch.
+context-parallel merge kernel on a decode batch, ``--op select_entries`` the
+grouped planner on the sparse verify shape.
 
 Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
 torchrun, each rank runs an independent replica (no collective on the data
@@ -701,6 +702,72 @@ def run_dcp_merge(args):
     print(json.dumps(line), flush=True)
 
 
+SEL_METRIC = "grouped planner µs per call (token-ID selections -> microblock entries + masks)"
+
+
+def run_select_entries(args):
+    """The grouped planner on the QSA verify shape: 4 requests x 4 query rows
+    x 2048 selected token positions over a 131072-token context."""
+    import numpy as np
+
+    from fp8_e4m3_paged_gb300 import binding as B
+    from fp8_e4m3_paged_gb300 import build_lib
+    from synth import make_selection
+
+    _, _, local = _dist()
+    torch.cuda.set_device(local)
+    build_lib.build()
+    Bn, q, topk, L = 4, 4, 2048, 131072
+    mb = L // 4
+    dev = torch.device("cuda")
+    sel = make_selection(Bn, q, L, topk, seed=5).to(dev)
+    bt = torch.from_numpy(np.random.default_rng(1).permutation(Bn * mb).astype(np.int32).reshape(Bn, mb)).to(dev)
+    stride = (q * topk + 7) // 8 * 8
+    tbl = torch.empty(Bn, stride, dtype=torch.int32, device=dev)
+    msk = torch.empty(Bn, stride, dtype=torch.int32, device=dev)
+    n = torch.empty(Bn, dtype=torch.int32, device=dev)
+    a = B.make_select_args(sel=sel, block_table=bt, max_blocks=mb, null_block=0, entry_tbl=tbl, entry_mask=msk,
+                           n_entries=n)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.fp8kv_attn_select_to_entries(a, s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(10):
+            B.fp8kv_attn_select_to_entries(a, torch.cuda.current_stream().cuda_stream)
+    reps = max(3, args.steps // 10)
+    with torch.cuda.stream(s):
+        for _ in range(max(3, args.warmup // 10)):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * 10)
+    alg = sel.numel() * 4 + int(n.sum().item()) * 8 + Bn * 4
+    peak, peak_src = _peaks()
+    print(json.dumps({
+        "op": "select_entries", "metric": SEL_METRIC, "value": round(us, 3), "unit": "us", "n_gpus": 1,
+        "steps": reps * 10, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic (seeded selections: runs of "
+        "neighbouring tokens, 10% unused slots, 5% duplicates)",
+        "config": {"workload": "select_entries: 4 requests x 4 rows x 2048 positions, context 131072 (32768 "
+                               "logical microblocks, 4 shared-memory chunks per request)",
+                   "entries_per_request": n.tolist(),
+                   "l2": "inputs (131 KB) stay in L2: a latency figure, not a bandwidth one"},
+        "roofline": {"bound": "hbm", "kernel": "select_entries", "achieved": round(alg / (us * 1e-6) / 1e9, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(alg / (us * 1e-6) / 1e9 / peak, 5),
+                     "traffic": None, "algorithmic_bytes_per_launch": alg, "avg_launch_us": round(us, 3),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+        "gpu_launches": reps * 10,
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -713,11 +780,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "cache_write", "dcp_merge"], default="attention")
+    ap.add_argument("--op", choices=["attention", "cache_write", "dcp_merge", "select_entries"], default="attention")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.op == "dcp_merge":
+    if args.op == "select_entries":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "select_entries",
+                              "unavailable": "the planner is timed on the GPU only; its oracle is pinned in tests"}))
+        else:
+            run_select_entries(args)
+    elif args.op == "dcp_merge":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "op": "dcp_merge",
                               "unavailable": "the merge is timed on the GPU only; its oracle is pinned in tests"}))

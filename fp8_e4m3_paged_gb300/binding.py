@@ -110,6 +110,16 @@ class MergeArgs(ctypes.Structure):
     ]
 
 
+class SelectArgs(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("q_max", ctypes.c_int32), ("topk", ctypes.c_int32),
+        ("max_blocks", ctypes.c_int32), ("null_block", ctypes.c_int32),
+        ("sel", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int64),
+        ("entry_tbl", ctypes.c_void_p), ("entry_mask", ctypes.c_void_p), ("entry_stride", ctypes.c_int64),
+        ("n_entries", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build it with `python -m fp8_e4m3_paged_gb300.build_lib` "
@@ -136,6 +146,8 @@ lib.fp8kv_attn_merge.restype = ctypes.c_int
 lib.fp8kv_attn_merge.argtypes = [ctypes.POINTER(MergeArgs), ctypes.c_void_p]
 lib.fp8kv_attn_merge_scale.restype = ctypes.c_int
 lib.fp8kv_attn_merge_scale.argtypes = [ctypes.POINTER(MergeArgs), ctypes.c_int32, ctypes.c_void_p]
+lib.fp8kv_attn_select_to_entries.restype = ctypes.c_int
+lib.fp8kv_attn_select_to_entries.argtypes = [ctypes.POINTER(SelectArgs), ctypes.c_void_p]
 lib.fp8kv_attn_cache_write.restype = ctypes.c_int
 lib.fp8kv_attn_cache_write.argtypes = [ctypes.POINTER(CacheWriteArgs), ctypes.c_void_p]
 
@@ -318,3 +330,24 @@ def fp8kv_attn_merge_scale(args: MergeArgs, rank: int, stream: int = 0) -> None:
     rc = lib.fp8kv_attn_merge_scale(ctypes.byref(args), rank, ctypes.c_void_p(stream))
     if rc != OK:
         raise Fp8kvError(rc, "fp8kv_attn_merge_scale")
+
+
+def make_select_args(*, sel, block_table, max_blocks: int, null_block: int, entry_tbl, entry_mask,
+                     n_entries, status=None) -> SelectArgs:
+    """sel: int32 [B][q][topk]; block_table: int32 [B][>= max_blocks];
+    entry_tbl / entry_mask: int32 [B][stride] (the mask tensor holds the
+    uint32 bit patterns); n_entries: int32 [B] (torch CUDA tensors)."""
+    a = SelectArgs()
+    a.batch, a.q_max, a.topk = sel.shape
+    a.max_blocks, a.null_block = max_blocks, null_block
+    a.sel = _ptr(sel)
+    a.block_table, a.block_table_stride = _ptr(block_table), block_table.stride(0)
+    a.entry_tbl, a.entry_mask, a.entry_stride = _ptr(entry_tbl), _ptr(entry_mask), entry_tbl.stride(0)
+    a.n_entries, a.status = _ptr(n_entries), _ptr(status)
+    return a
+
+
+def fp8kv_attn_select_to_entries(args: SelectArgs, stream: int = 0) -> None:
+    rc = lib.fp8kv_attn_select_to_entries(ctypes.byref(args), ctypes.c_void_p(stream))
+    if rc != OK:
+        raise Fp8kvError(rc, "fp8kv_attn_select_to_entries")

@@ -304,3 +304,16 @@ extern "C" int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, f
   const cudaError_t e = launch_merge(*a, rank, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
 }
+
+extern "C" int fp8kv_attn_select_to_entries(const fp8kv_select_args* a, fp8kv_stream_t stream) {
+  if (!a) return FP8KV_EINVAL;
+  if (a->batch < 0 || a->q_max < 1 || a->q_max > 8 || a->topk < 0 || a->max_blocks < 1) return FP8KV_EINVAL;
+  if (a->block_table_stride < a->max_blocks) return FP8KV_EINVAL;
+  const int64_t cap = ((int64_t)a->q_max * a->topk + 7) / 8 * 8;
+  if (a->entry_stride < cap || a->entry_stride < 1) return FP8KV_EINVAL;
+  if (a->batch == 0) return FP8KV_OK;
+  if ((a->topk > 0 && !a->sel) || !a->block_table || !a->entry_tbl || !a->entry_mask || !a->n_entries)
+    return FP8KV_EINVAL;
+  const cudaError_t e = launch_select_to_entries(*a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;
+}

@@ -58,6 +58,7 @@ cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cuda
 cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_cache_write(const fp8kv_cache_write_args& a, cudaStream_t s);
 cudaError_t launch_merge(const fp8kv_merge_args& a, int32_t scale_rank, cudaStream_t s);
+cudaError_t launch_select_to_entries(const fp8kv_select_args& a, cudaStream_t s);
 
 // Runs a setup call (a kernel attribute) once per device, on first use.
 struct DeviceOnce {

@@ -280,6 +280,40 @@ int fp8kv_attn_combine_lse(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args*
 int fp8kv_attn_merge(const fp8kv_merge_args* a, fp8kv_stream_t stream);
 int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, fp8kv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Grouped planner: token-ID selections -> the sparse mode's entries.
+ *
+ * For every request b: the distinct four-token logical microblocks
+ * m = t / 4 that any query row selected (positions t >= 0, below
+ * 4 * max_blocks), in increasing order, become entries with
+ *   entry_tbl[b][e]  = block_table[b][m]          (physical microblock)
+ *   entry_mask[b][e] = OR over selections t of row r in m of bit 4r + t%4
+ * and null entries (null_block, mask 0) pad the count to a multiple of 8;
+ * n_entries[b] is the padded count ("Qualify calibrated E4M3 and disk PLE
+ * with QSA DCP2", commit "grouped page4 null-block padding").  Duplicate
+ * selections are harmless; negative positions are unused slots; positions
+ * at or past 4 * max_blocks are ignored and set FP8KV_STATUS_BAD_ENTRIES in
+ * *status (when not NULL).  Entries past n_entries[b] are not written.
+ * Device-side and graph-capturable: the counts never reach the host.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t batch;                /* B >= 0 */
+  int32_t q_max;                /* query rows per request, 1..8 (32-bit masks) */
+  int32_t topk;                 /* selection slots per row, >= 0 */
+  int32_t max_blocks;           /* logical microblocks per request, >= 1 */
+  int32_t null_block;           /* physical microblock of padding entries */
+  const int32_t* sel;           /* [B][q_max][topk] token positions, < 0 = unused */
+  const int32_t* block_table;   /* [B][block_table_stride] logical -> physical microblock */
+  int64_t block_table_stride;   /* elements, >= max_blocks */
+  int32_t* entry_tbl;           /* [B][entry_stride] */
+  uint32_t* entry_mask;         /* [B][entry_stride] */
+  int64_t entry_stride;         /* elements, >= q_max * topk rounded up to 8 */
+  int32_t* n_entries;           /* [B] */
+  uint32_t* status;             /* optional status word, NULL = none */
+} fp8kv_select_args;
+
+int fp8kv_attn_select_to_entries(const fp8kv_select_args* a, fp8kv_stream_t stream);
+
 /* Size of the library-owned device scratch used by fp8kv_attn_forward_static
  * (16 MiB; one copy per GPU that loads the library, held until exit). */
 #define FP8KV_STATIC_SCRATCH_BYTES (16u << 20)

@@ -17,6 +17,11 @@ Parity status of each exported function (what pins it, in ``tests/``):
                       equal-logit closed forms of the LSE
   merge               one rank is the identity, an empty rank changes
                       nothing, shards of one problem merge to the whole
+  select_to_entries   hand-worked golden case, invariants (every selection
+                      visible exactly once, no other bit, increasing order,
+                      null padding to x8), and sparse attention over the
+                      result equal to a direct per-row softmax over the
+                      selected tokens
   cache write         slot placement, skipped and out-of-range slots,
                       strides, decode(write(x)) within half a quantum of
                       x / scale, power-of-two scales against the encoder
@@ -290,3 +295,50 @@ def merge(outs, lses, plant: int = 0):
     lm = np.zeros(l.shape[1:], dtype=np.float64)
     load(plant).orc_merge(R, n, D, o.ctypes.data, l.ctypes.data, m.ctypes.data, lm.ctypes.data)
     return m, lm
+
+
+def select_to_entries(sel, block_table, max_blocks: int, null_block: int, entry_stride: Optional[int] = None):
+    """The grouped planner, from its definition ("Qualify calibrated E4M3 and
+    disk PLE with QSA DCP2", commit "grouped page4 null-block padding").
+
+    sel: int [B][q][topk] token positions of each request's query rows (< 0 =
+    unused; positions at or past 4 * max_blocks are ignored and counted).
+    For each request: the distinct four-token logical microblocks m = t // 4
+    any row selected, in increasing order; entry_tbl = block_table[b][m];
+    bit 4r + t % 4 of entry_mask set iff row r selected token t; then null
+    entries (null_block, mask 0) up to a multiple of 8.
+    Returns (entry_tbl [B][stride] int32, entry_mask [B][stride] uint32,
+    n_entries [B] int32, n_ignored)."""
+    sel = np.asarray(sel, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    B, q, _ = sel.shape
+    ignored = 0
+    per_req = []
+    for b in range(B):
+        toks = []
+        for r in range(q):
+            for t in sel[b, r]:
+                if t < 0:
+                    continue
+                if t >= 4 * max_blocks:
+                    ignored += 1
+                    continue
+                toks.append((int(t), r))
+        mbs = np.unique(np.array([t // 4 for t, _ in toks], dtype=np.int64))  # sorted, distinct
+        masks = {int(m): 0 for m in mbs}
+        for t, r in toks:
+            masks[t // 4] |= 1 << (4 * r + t % 4)
+        ent = [(int(bt[b, m]), masks[int(m)]) for m in mbs]
+        ent += [(null_block, 0)] * ((-len(ent)) % 8)
+        per_req.append(ent)
+    stride = entry_stride or max(8, max(len(e) for e in per_req))
+    tbl = np.zeros((B, stride), dtype=np.int32)
+    msk = np.zeros((B, stride), dtype=np.uint32)
+    n = np.zeros(B, dtype=np.int32)
+    for b, ent in enumerate(per_req):
+        assert len(ent) <= stride, "entries exceed the stride"
+        n[b] = len(ent)
+        for e, (t, m) in enumerate(ent):
+            tbl[b, e] = t
+            msk[b, e] = m
+    return tbl, msk, n, ignored

@@ -2,7 +2,8 @@
 
 This package only *makes data*: query vectors, E4M3 key/value page pools,
 block tables, per-row live lengths, QSA microblock tables with visibility
-masks, and new fp16/bf16 K/V rows with their cache slots.  It contains none
+masks, token-ID selections, and new fp16/bf16 K/V rows with their cache
+slots.  It contains none
 of the attention or quantisation arithmetic, and it is the only code shared
 by the CPU oracle (``oracle/``) and the CUDA library
 (``fp8_e4m3_paged_gb300``).
@@ -18,3 +19,4 @@ from .workloads import (  # noqa: F401
     attended_kv_bytes,
 )
 from .cache_write import CacheWriteProblem, make_cache_write  # noqa: F401
+from .selection import make_selection  # noqa: F401

@@ -357,7 +357,9 @@ def make_sparse(
         softmax_scale=float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
         k_scale=float(ks), v_scale=float(vs), max_kv_len=L,
         entry_tbl=entry_tbl, entry_mask=entry_mask, n_entries=n_entries,
-        meta={"L": L, "topk_blocks": topk_blocks, "seed": seed},
+        meta={"L": L, "topk_blocks": topk_blocks, "seed": seed,
+              # logical microblock -> physical microblock of every request
+              "block_table": phys_of.to(torch.int32)},
     )
 
 

@@ -178,3 +178,29 @@ def test_cache_write_empty_and_null(B):
     assert B.lib.fp8kv_attn_cache_write(None, None) == B.EINVAL
     # no tokens: nothing to launch, pointers may be null
     assert B.lib.fp8kv_attn_cache_write(ctypes.byref(_cw(B, num_tokens=0, k=0, v=0)), None) == B.OK
+
+
+# ------------------------------------------------------------------ grouped planner (host validation only)
+
+def _sel(B, **kw):
+    a = B.SelectArgs()
+    a.batch, a.q_max, a.topk, a.max_blocks, a.null_block = 2, 4, 16, 100, 0
+    a.sel = a.block_table = a.entry_tbl = a.entry_mask = a.n_entries = 0x10000  # never dereferenced
+    a.block_table_stride, a.entry_stride = 100, 64
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(batch=-1), dict(q_max=0), dict(q_max=9), dict(topk=-1), dict(max_blocks=0),
+    dict(block_table_stride=99), dict(entry_stride=63), dict(sel=0), dict(block_table=0), dict(entry_tbl=0),
+    dict(entry_mask=0), dict(n_entries=0),
+])
+def test_select_to_entries_rejects_bad_arguments(B, bad):
+    assert B.lib.fp8kv_attn_select_to_entries(ctypes.byref(_sel(B, **bad)), None) == B.EINVAL
+
+
+def test_select_to_entries_empty_batch(B):
+    assert B.lib.fp8kv_attn_select_to_entries(None, None) == B.EINVAL
+    assert B.lib.fp8kv_attn_select_to_entries(ctypes.byref(_sel(B, batch=0, sel=0, n_entries=0)), None) == B.OK
