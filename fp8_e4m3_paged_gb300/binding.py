@@ -15,7 +15,7 @@ from typing import Optional
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8kv_attn.so")
 
-REVISION = 1
+REVISION = 2
 OK = 0
 EINVAL = -1
 EUNSUPPORTED = -2
@@ -25,6 +25,9 @@ ECUDA = -5
 
 MODE_DENSE = 0
 MODE_SPARSE_PAGE4 = 1
+
+KV_E4M3 = 0
+KV_E5M2 = 1
 
 KERNEL_AUTO = 0
 KERNEL_GENERIC = 1
@@ -39,7 +42,7 @@ STATUS_TIMEOUT = 0x8
 class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "batch", "q_max", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
-        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits", "kernel")]
+        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits", "kernel", "kv_format")]
 
 
 class Plan(ctypes.Structure):
@@ -52,7 +55,8 @@ class Plan(ctypes.Structure):
         ("row_chunk", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("partial_offset", ctypes.c_int64), ("ml_offset", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
-        ("reserved", ctypes.c_int32 * 16),
+        ("kv_format", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 15),
     ]
 
 
@@ -197,9 +201,10 @@ def fp8kv_attn_forward_static(plan: Plan, args: Args, stream: int = 0) -> None:
 
 def make_desc(*, mode: int, batch: int, q_max: int, num_q_heads: int, num_kv_heads: int,
               head_dim: int, page_size: int, max_kv_len: int, max_blocks: int,
-              num_kv_blocks: int, num_sms: int = 0, num_splits: int = 0, kernel: int = 0) -> Desc:
+              num_kv_blocks: int, num_sms: int = 0, num_splits: int = 0, kernel: int = 0,
+              kv_format: int = KV_E4M3) -> Desc:
     return Desc(mode, batch, q_max, num_q_heads, num_kv_heads, head_dim, page_size,
-                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits, kernel)
+                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits, kernel, kv_format)
 
 
 def _ptr(t) -> Optional[int]:

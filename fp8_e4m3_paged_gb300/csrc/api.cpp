@@ -47,6 +47,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   if (d->num_sms < 0 || d->num_splits < 0) return FP8KV_EINVAL;
   if (d->kernel < FP8KV_KERNEL_AUTO || d->kernel > FP8KV_KERNEL_TC) return FP8KV_EINVAL;
   if (d->kernel == FP8KV_KERNEL_TC && d->head_dim != 128 && d->head_dim != 256) return FP8KV_EUNSUPPORTED;
+  if (d->kv_format != FP8KV_KV_E4M3 && d->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
   if (d->mode == FP8KV_MODE_DENSE) {
     if ((int64_t)d->max_blocks * d->page_size < d->max_kv_len) return FP8KV_EINVAL;
   } else {
@@ -78,6 +79,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   P.group = d->num_q_heads / d->num_kv_heads;
   P.rows = d->q_max * P.group;
   P.num_sms = sms;
+  P.kv_format = d->kv_format;
 
   // Kernel choice: the tcgen05 path when the grouped rows fill at least a
   // quarter of its 64-row MMA tile and D is 128 or 256; otherwise the generic
@@ -156,6 +158,8 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->max_kv_len = plan->max_kv_len;
   p->max_blocks = plan->max_blocks;
   p->num_kv_blocks = plan->num_kv_blocks;
+  p->kv_format = plan->kv_format;
+  if (p->kv_format != FP8KV_KV_E4M3 && p->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
   if (p->G < 1 || p->rows != p->q_max * p->G || p->S < 1 || p->row_chunk < 1) return FP8KV_EINVAL;
 
   if (!a->workspace || !aligned(a->workspace, 256)) return FP8KV_EINVAL;

@@ -5,7 +5,9 @@
 //
 // written as fp16 with round-to-nearest-even.  A query vector whose total L is
 // 0 (dead row, or nothing visible) gets +0.0.  Partitions with l_s = 0 are
-// dropped by selection, so their numerators are never used.  The partition
+// dropped by selection, so their numerators are never used; a NaN l_s (a NaN
+// byte in a token some row sees) is kept, so the NaN reaches the output as
+// the exact softmax would have it.  The partition
 // maxima are integers (base-2 units), so every w_s is an exact power of two
 // ("DFlash2 E4M3 attention with FP32 state", intro paragraph 4: FP32
 // combination, FP16 final activation; "Qwen4Exp: fp8_e4m3 main KV cache on
@@ -96,10 +98,10 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
       float M0 = -INFINITY;
 #pragma unroll
       for (int k = 0; k < KR; ++k)
-        if (lv[k] > 0.f) M0 = fmaxf(M0, mv[k]);
+        if (lv[k] != 0.f) M0 = fmaxf(M0, mv[k]);
       for (int s = tid + MAXS; s < S; s += CT) {
         const float2 v = ml[s * sstride];
-        if (v.y > 0.f) M0 = fmaxf(M0, v.x);
+        if (v.y != 0.f) M0 = fmaxf(M0, v.x);
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) M0 = fmaxf(M0, __shfl_xor_sync(0xffffffffu, M0, off));
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
     for (int k = 0; k < KR; ++k) {
       const int kk = tid + k * CT;
       if (kk < ns) {
-        const bool live = lv[k] > 0.f;
+        const bool live = lv[k] != 0.f;
         s_w[kk] = live ? exp2_int(mv[k] - M) : 0.f;  // integer maxima: exact
         s_l[kk] = live ? lv[k] : 0.f;
       }
@@ -174,14 +176,15 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
       Lt += red_l[k];
     }
     const float vs = p.v_scale_dev ? *p.v_scale_dev : p.v_scale;
-    const float f = (Lt > 0.f) ? vs / Lt : 0.f;
-    const float y0 = (Lt > 0.f) ? t.x * f : 0.f;
-    const float y1 = (Lt > 0.f) ? t.y * f : 0.f;
-    const float y2 = (Lt > 0.f) ? t.z * f : 0.f;
-    const float y3 = (Lt > 0.f) ? t.w * f : 0.f;
+    const bool any = Lt != 0.f;  // NaN (a NaN byte in a seen token) propagates
+    const float f = any ? vs / Lt : 0.f;
+    const float y0 = any ? t.x * f : 0.f;
+    const float y1 = any ? t.y * f : 0.f;
+    const float y2 = any ? t.z * f : 0.f;
+    const float y3 = any ? t.w * f : 0.f;
     if (LSE) {
       *reinterpret_cast<float4*>(p.out_f32 + (int64_t)idx * D + slice * DW + tid * 4) = make_float4(y0, y1, y2, y3);
-      if (slice == 0 && tid == 0) p.lse[idx] = (Lt > 0.f) ? M + log2f(Lt) : -INFINITY;
+      if (slice == 0 && tid == 0) p.lse[idx] = any ? M + log2f(Lt) : -INFINITY;
       return;
     }
     const __half2 h01 = __floats2half2_rn(y0, y1);

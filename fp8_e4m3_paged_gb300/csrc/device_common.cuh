@@ -16,14 +16,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 // the FP32 exponent field and mmm in the top of the FP32 mantissa encodes
 // dec(b) * 2^-120 exactly (normal codes: 2^(e-127) * 1.mmm; subnormal codes
 // e = 0: m * 2^-129 as an FP32 denormal); multiplying by 2^120 is exact.
-// The two NaN codes map to the finite value 480: every byte the kernels read
-// but must not use is excluded by selection, never by arithmetic.
+// The two NaN codes give NaN (the placement alone would give 480).  Every
+// byte the kernels read but must not use is excluded by selection, never by
+// arithmetic, so a NaN code only matters in a token some row attends.
 __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&o)[4]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint32_t b = (w >> (8 * k)) & 0xFFu;
     const uint32_t bits = ((b & 0x80u) << 24) | ((b & 0x7Fu) << 20);
-    o[k] = __uint_as_float(bits) * 0x1p120f;
+    // 0x7F / 0xFF are NaN in E4M3FN (the bit placement would give 480)
+    o[k] = ((b & 0x7Fu) == 0x7Fu) ? __uint_as_float(0x7FC00000u) : __uint_as_float(bits) * 0x1p120f;
+  }
+}
+
+// Four E5M2 bytes -> four floats: an E5M2 byte is the upper byte of the
+// IEEE binary16 with the same value (infinities and NaNs included).
+__device__ __forceinline__ void e5m2x4_to_f32(uint32_t w, float (&o)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned short h = (unsigned short)(((w >> (8 * k)) & 0xFFu) << 8);
+    o[k] = __half2float(__ushort_as_half(h));
   }
 }
 

@@ -202,12 +202,19 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
       float f[4];
       const uint32_t kwa[4] = {kw.x, kw.y, kw.z, kw.w};
       const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
+      const bool e5 = p.kv_format == FP8KV_KV_E5M2;  // uniform
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        e4m3x4_to_f32(kwa[j], f);
+        if (e5)
+          e5m2x4_to_f32(kwa[j], f);
+        else
+          e4m3x4_to_f32(kwa[j], f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) Ks[t * (D + 1) + vv * 16 + j * 4 + k] = f[k];
-        e4m3x4_to_f32(vwa[j], f);
+        if (e5)
+          e5m2x4_to_f32(vwa[j], f);
+        else
+          e4m3x4_to_f32(vwa[j], f);
         *reinterpret_cast<float4*>(&Vs[t * D + vv * 16 + j * 4]) = make_float4(f[0], f[1], f[2], f[3]);
       }
     }

@@ -204,16 +204,26 @@ __device__ __forceinline__ void st_16x128b_x8_pair(uint32_t taddr_hi, uint32_t t
 // Exact E4M3 -> fp16 for two bytes (hardware conversion): dec(b) itself;
 // |dec| <= 448 and the subnormal quantum 2^-9 are both exact in fp16.
 // Four E4M3 bytes (little-endian in w) -> two fp16 pairs (bytes 0,1 and 2,3).
+template <int FMT>
 __device__ __forceinline__ void cvt4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
+  if (FMT == FP8KV_KV_E5M2) {
+    // E5M2 -> fp16 is exact too (the byte is the upper byte of the binary16)
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, a;\n\tcvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  } else {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  }
 }
+template <int FMT>
 __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
   uint4 r;
-  cvt4(a, r.x, r.y);
-  cvt4(b, r.z, r.w);
+  cvt4<FMT>(a, r.x, r.y);
+  cvt4<FMT>(b, r.z, r.w);
   return r;
 }
 
@@ -225,7 +235,7 @@ __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
 // is a per-thread base plus a compile-time offset; all loads are issued
 // before the first conversion.  Rows whose bit in `valid` is clear were not
 // copied and become zeros.
-template <int D, int DBS>
+template <int D, int DBS, int FMT>
 __device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uint64_t valid, int lt) {
   constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
   constexpr int kR = kDecThreads / kChunks; // rows per pass
@@ -252,7 +262,7 @@ __device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uin
   for (int k = 0; k < kPer; ++k) {
     const int sw = (t0 + k * kR) & 7;
     uint8_t* row = dst + k * kR * 128;
-    const uint4 x0 = dec8(w[k].x, w[k].y), x1 = dec8(w[k].z, w[k].w);
+    const uint4 x0 = dec8<FMT>(w[k].x, w[k].y), x1 = dec8<FMT>(w[k].z, w[k].w);
     *reinterpret_cast<uint4*>(row + ((first ^ sw) * 16)) = swap ? x1 : x0;
     *reinterpret_cast<uint4*>(row + ((second ^ sw) * 16)) = swap ? x0 : x1;
   }
@@ -312,7 +322,7 @@ __device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* ca
 
 // ---------------------------------------------------------------- the kernel
 
-template <int D, int MODE>
+template <int D, int MODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -508,9 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         // K stages hold pairs of tiles interleaved per column block, so that
         // two consecutive tiles form one 128-row operand of the pair's QK
         uint8_t* op = op_base + (st / 2) * (2 * C::kOpBytes) + (st % 2) * (kT * 128);
-        decode_tile<D, 2 * kT * 128>(raw_base + slot * C::kRawBytes, op, valid[slot], lt);
+        decode_tile<D, 2 * kT * 128, FMT>(raw_base + slot * C::kRawBytes, op, valid[slot], lt);
       } else {
-        decode_tile<D, kT * 128>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
+        decode_tile<D, kT * 128, FMT>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
       }
       fence_proxy_async_smem();
       mbar_arrive(&op_full[st / 2]);
@@ -793,9 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   }
 }
 
-template <int D, int MODE>
+template <int D, int MODE, int FMT>
 cudaError_t launch(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t st) {
-  auto fn = split_tc<D, MODE>;
+  auto fn = split_tc<D, MODE, FMT>;
   static DeviceOnce once;
   cudaError_t e = once.run([&] {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
@@ -810,14 +820,20 @@ cudaError_t launch(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t 
 
 int tc_smem_bytes(int D) { return D == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
 
-cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t st) {
+template <int FMT>
+cudaError_t launch_fmt(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t st) {
   if (p.D == 256)
-    return p.mode == FP8KV_MODE_DENSE ? launch<256, FP8KV_MODE_DENSE>(plan, p, st)
-                                      : launch<256, FP8KV_MODE_SPARSE_PAGE4>(plan, p, st);
+    return p.mode == FP8KV_MODE_DENSE ? launch<256, FP8KV_MODE_DENSE, FMT>(plan, p, st)
+                                      : launch<256, FP8KV_MODE_SPARSE_PAGE4, FMT>(plan, p, st);
   if (p.D == 128)
-    return p.mode == FP8KV_MODE_DENSE ? launch<128, FP8KV_MODE_DENSE>(plan, p, st)
-                                      : launch<128, FP8KV_MODE_SPARSE_PAGE4>(plan, p, st);
+    return p.mode == FP8KV_MODE_DENSE ? launch<128, FP8KV_MODE_DENSE, FMT>(plan, p, st)
+                                      : launch<128, FP8KV_MODE_SPARSE_PAGE4, FMT>(plan, p, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t st) {
+  return p.kv_format == FP8KV_KV_E5M2 ? launch_fmt<FP8KV_KV_E5M2>(plan, p, st)
+                                      : launch_fmt<FP8KV_KV_E4M3>(plan, p, st);
 }
 
 }  // namespace fp8kv

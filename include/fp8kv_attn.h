@@ -10,7 +10,8 @@
  *   z_j   = softmax_scale * k_scale * <q[b][r][h], dec(K_j)>
  *   out   = v_scale * sum_j softmax(z)_j * dec(V_j)          (fp16, RNE)
  *
- * where dec() is the exact E4M3 (OCP E4M3FN) decode of the cache bytes.
+ * where dec() is the exact decode of the cache bytes: E4M3 (OCP E4M3FN), or
+ * E5M2 when the plan's kv_format says so.
  *  - Dense mode: row r sees tokens [0, row_kv_len[b][r]); token t lives in
  *    physical block block_table[b][t / page_size], slot t % page_size.  A row
  *    length of 0 is a dead row and yields +0.0.  (Live per-query lengths
@@ -68,7 +69,7 @@ extern "C" {
  * stale plan cannot reach kernels with another partial layout ("DFlash2 E4M3
  * attention with FP32 state", intro paragraph 5: the wrapper requires a given
  * precision capability revision). */
-#define FP8KV_ATTN_REVISION 1
+#define FP8KV_ATTN_REVISION 2
 
 /* Return codes. */
 #define FP8KV_OK 0
@@ -81,6 +82,13 @@ extern "C" {
 /* Modes. */
 #define FP8KV_MODE_DENSE 0
 #define FP8KV_MODE_SPARSE_PAGE4 1
+
+/* Cache byte formats (desc.kv_format).  E4M3: OCP E4M3FN (no infinity,
+ * 0x7F/0xFF NaN, largest 448).  E5M2: the upper byte of an IEEE binary16
+ * (infinities and NaNs as in binary16, largest finite 57344) -- the legacy
+ * format of the kernels "DFlash2 E4M3 attention with FP32 state" replaces. */
+#define FP8KV_KV_E4M3 0
+#define FP8KV_KV_E5M2 1
 
 /* Split-kernel choice (desc.kernel; the plan records the one chosen). */
 #define FP8KV_KERNEL_AUTO 0
@@ -112,6 +120,7 @@ typedef struct {
   int32_t num_sms;       /* SMs to plan for; 0 = ask the current device */
   int32_t num_splits;    /* split-KV partitions per (request, KV head); 0 = planner's choice */
   int32_t kernel;        /* FP8KV_KERNEL_*: 0 = planner's choice */
+  int32_t kv_format;     /* FP8KV_KV_*: 0 = E4M3 */
 } fp8kv_attn_desc;
 
 /* A plan: plain data, owned by the caller, nothing to free.  Fields other than
@@ -133,7 +142,8 @@ typedef struct {
   int64_t partial_offset;  /* byte offset of FP32 numerators in the workspace */
   int64_t ml_offset;       /* byte offset of FP32 (max, sum) pairs */
   int64_t workspace_bytes; /* minimum workspace size */
-  int32_t reserved[16];
+  int32_t kv_format;       /* FP8KV_KV_* of the cache bytes */
+  int32_t reserved[15];
 } fp8kv_attn_plan_t;
 
 /* Per-call arguments.  All pointers are device pointers owned by the caller,

@@ -9,6 +9,8 @@ it with ctypes.  Inputs are ``synth.Problem`` objects (CPU tensors).
 
 Parity status of each exported function (what pins it, in ``tests/``):
   e4m3 table          format definition closed form + torch float8_e4m3fn
+  e5m2 table          format definition (binary16 upper byte) + torch
+                      float8_e5m2, all 256 codes
   e4m3 encode         round trip of every code, exact midpoints (ties to
                       even), nearest on both sides of each midpoint,
                       saturation, signed zero, torch float8_e4m3fn in range
@@ -85,7 +87,7 @@ class OrcProblem(ctypes.Structure):
         ("entry_tbl", ctypes.c_void_p), ("entry_mask", ctypes.c_void_p),
         ("n_entries", ctypes.c_void_p), ("entry_stride", ctypes.c_int64),
         ("softmax_scale", ctypes.c_double), ("k_scale", ctypes.c_double),
-        ("v_scale", ctypes.c_double),
+        ("v_scale", ctypes.c_double), ("kv_format", ctypes.c_int),
     ]
 
 
@@ -101,6 +103,9 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.orc_e4m3.restype = ctypes.c_double
     lib.orc_e4m3.argtypes = [ctypes.c_uint8]
     lib.orc_e4m3_table.argtypes = [ctypes.c_void_p]
+    lib.orc_e5m2.restype = ctypes.c_double
+    lib.orc_e5m2.argtypes = [ctypes.c_uint8]
+    lib.orc_e5m2_table.argtypes = [ctypes.c_void_p]
     lib.orc_f16.restype = ctypes.c_double
     lib.orc_f16.argtypes = [ctypes.c_uint16]
     lib.orc_attention.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
@@ -172,12 +177,19 @@ class _Pinned:
         s.softmax_scale = p.softmax_scale
         s.k_scale = p.k_scale
         s.v_scale = p.v_scale
+        s.kv_format = 1 if getattr(p, "kv_format", "e4m3") == "e5m2" else 0
         self.s = s
 
 
 def e4m3_table(plant: int = 0) -> np.ndarray:
     out = np.zeros(256, dtype=np.float64)
     load(plant).orc_e4m3_table(out.ctypes.data)
+    return out
+
+
+def e5m2_table(plant: int = 0) -> np.ndarray:
+    out = np.zeros(256, dtype=np.float64)
+    load(plant).orc_e5m2_table(out.ctypes.data)
     return out
 
 

@@ -68,6 +68,7 @@ typedef struct {
   const int32_t* n_entries;      // sparse: [B]
   int64_t entry_stride;
   double softmax_scale, k_scale, v_scale;
+  int kv_format;  // cache byte format: 0 = E4M3 (E4M3FN), 1 = E5M2
 } orc_problem;
 
 // ORC_PLANT (compile-time, default 0 = none) plants one plausible mistake;
@@ -99,6 +100,35 @@ ORC_API double orc_e4m3(uint8_t b) {
 ORC_API void orc_e4m3_table(double* out256) {
   for (int i = 0; i < 256; ++i) out256[i] = orc_e4m3((uint8_t)i);
 }
+
+// E5M2 byte -> value, from the format definition: 1 sign, 5 exponent bits
+// (bias 15), 2 mantissa bits, subnormals, infinities (exponent 31, mantissa
+// 0) and NaN (exponent 31, mantissa != 0) as in IEEE binary16, of which it
+// is the upper byte -- the legacy cache format of "DFlash2 E4M3 attention
+// with FP32 state" (the E5M2 kernels the page replaces).
+ORC_API double orc_e5m2(uint8_t b) {
+  const int s = b >> 7;
+  const int e = (b >> 2) & 31;
+  const int m = b & 3;
+  double v;
+  if (e == 31)
+    v = m ? std::numeric_limits<double>::quiet_NaN() : std::numeric_limits<double>::infinity();
+  else if (e == 0)
+    v = std::ldexp((double)m, -16);  // m/4 * 2^(1-15)
+  else
+    v = std::ldexp(1.0 + (double)m / 4.0, e - 15);
+#if ORC_PLANT == 14
+  if (e != 0 && e != 31) v = std::ldexp(1.0 + (double)m / 4.0, e - 16);  // planted: bias 16
+#endif
+  return s ? -v : v;
+}
+
+ORC_API void orc_e5m2_table(double* out256) {
+  for (int i = 0; i < 256; ++i) out256[i] = orc_e5m2((uint8_t)i);
+}
+
+// The problem's cache byte decode.
+static inline double dec(const orc_problem* p, uint8_t b) { return p->kv_format == 1 ? orc_e5m2(b) : orc_e4m3(b); }
 
 // IEEE binary16 bits -> value.
 ORC_API double orc_f16(uint16_t h) {
@@ -248,7 +278,7 @@ static void logits(const orc_problem* p, int b, int r, int h, const std::vector<
   for (size_t j = 0; j < toks.size(); ++j) {
     const uint8_t* kb = p->k_cache + toks[j].k_off;
     double dot = 0.0;
-    for (int d = 0; d < D; ++d) dot += qd[d] * orc_e4m3(kb[d]);
+    for (int d = 0; d < D; ++d) dot += qd[d] * dec(p, kb[d]);
     double sc = p->softmax_scale * p->k_scale;
 #if ORC_PLANT == 2
     sc = p->softmax_scale;  // planted: k_scale dropped
@@ -300,7 +330,7 @@ static void row_head_abs(const orc_problem* p, int b, int r, int h, double* out)
   for (size_t j = 0; j < toks.size(); ++j) {
     const double w = std::exp(z[j] - M) / S;
     const uint8_t* vb = p->v_cache + toks[j].v_off;
-    for (int d = 0; d < D; ++d) acc[d] += w * std::fabs(orc_e4m3(vb[d]));
+    for (int d = 0; d < D; ++d) acc[d] += w * std::fabs(dec(p, vb[d]));
   }
   for (int d = 0; d < D; ++d) out[d] = std::fabs(p->v_scale) * acc[d];
 }
@@ -328,7 +358,7 @@ static void row_head(const orc_problem* p, int b, int r, int h, double* out) {
 #else
     const uint8_t* vb = p->v_cache + toks[j].v_off;
 #endif
-    for (int d = 0; d < D; ++d) acc[d] += w * orc_e4m3(vb[d]);
+    for (int d = 0; d < D; ++d) acc[d] += w * dec(p, vb[d]);
   }
   double vs = p->v_scale;
 #if ORC_PLANT == 5
@@ -360,7 +390,7 @@ static void row_head_split(const orc_problem* p, int b, int r, int h, int S_, do
       const double e = std::exp(z[j] - m[s]);
       l[s] += e;
       const uint8_t* vb = p->v_cache + toks[j].v_off;
-      for (int d = 0; d < D; ++d) num[(size_t)s * D + d] += e * orc_e4m3(vb[d]);
+      for (int d = 0; d < D; ++d) num[(size_t)s * D + d] += e * dec(p, vb[d]);
     }
   }
   double M = -std::numeric_limits<double>::infinity();
@@ -382,6 +412,7 @@ static int check(const orc_problem* p) {
   if (!p || p->B < 0 || p->q < 1 || p->Hq < 1 || p->Hkv < 1 || p->D < 1) return -1;
   if (p->Hq % p->Hkv) return -1;
   if (p->mode == 1 && p->q > 8) return -1;
+  if (p->kv_format != 0 && p->kv_format != 1) return -1;
   return 0;
 }
 

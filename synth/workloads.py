@@ -45,6 +45,8 @@ from typing import Optional
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
+FMT_MAX = {"e4m3": E4M3_MAX, "e5m2": E5M2_MAX}
 POISON_NAN = 0x7F      # E4M3 NaN
 POISON_MAX = 0x7E      # E4M3 +448: finite, so only true exclusion survives it
 
@@ -85,6 +87,7 @@ class Problem:
     entry_mask: Optional[torch.Tensor] = None
     n_entries: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
+    kv_format: str = "e4m3"       # cache byte format: "e4m3" (E4M3FN) or "e5m2"
 
     @property
     def num_blocks(self) -> int:
@@ -124,6 +127,15 @@ def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
     """Quantise fp32 values x/scale to E4M3 bytes (RNE, clamped to +-448)."""
     y = (x / scale).clamp_(-E4M3_MAX, E4M3_MAX)
     return y.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def quantize_fp8(x: torch.Tensor, scale: float, kv_format: str = "e4m3") -> torch.Tensor:
+    """Cache bytes of x/scale in the given format (torch's RNE conversion
+    after clamping to the finite range)."""
+    if kv_format == "e4m3":
+        return quantize_e4m3(x, scale)
+    y = (x / scale).clamp_(-E5M2_MAX, E5M2_MAX)
+    return y.to(torch.float8_e5m2).view(torch.uint8)
 
 
 def _gauss(key: int, shape, outliers: bool) -> torch.Tensor:
@@ -176,6 +188,7 @@ def make_dense(
     poison: int = POISON_NAN,
     row_len=None,
     extra_pages: int = 0,
+    kv_format: str = "e4m3",
 ) -> Problem:
     """Build a dense paged problem.
 
@@ -216,8 +229,8 @@ def make_dense(
                 continue
             kmax = max(kmax, float(draw(b, 0).abs().max()))
             vmax = max(vmax, float(draw(b, 1).abs().max()))
-        ks = kmax / E4M3_MAX if kmax > 0 else 1.0
-        vs = vmax / E4M3_MAX if vmax > 0 else 1.0
+        ks = kmax / FMT_MAX[kv_format] if kmax > 0 else 1.0
+        vs = vmax / FMT_MAX[kv_format] if vmax > 0 else 1.0
         q_k, q_v = ks, vs
     elif value_mode == "direct":
         ks = float(k_scale)
@@ -230,8 +243,8 @@ def make_dense(
         L = lens[b]
         if L == 0:
             continue
-        kb = quantize_e4m3(draw(b, 0), q_k)
-        vb = quantize_e4m3(draw(b, 1), q_v)
+        kb = quantize_fp8(draw(b, 0), q_k, kv_format)
+        vb = quantize_fp8(draw(b, 1), q_v, kv_format)
         full = L // page_size
         if full:
             ids = block_table[b, :full].long()
@@ -256,7 +269,7 @@ def make_dense(
         softmax_scale=float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
         k_scale=float(ks), v_scale=float(vs), max_kv_len=max(lens) if lens else 0,
         block_table=block_table, row_len=rl,
-        meta={"lens": lens, "seed": seed},
+        meta={"lens": lens, "seed": seed}, kv_format=kv_format,
     )
 
 
@@ -279,6 +292,7 @@ def make_sparse(
     outliers: bool = False,
     softmax_scale: Optional[float] = None,
     pad_to: int = 8,
+    kv_format: str = "e4m3",
 ) -> Problem:
     """Build a QSA sparse problem over 4-token microblocks.
 
@@ -303,12 +317,12 @@ def make_sparse(
 
     kmax = max(float(draw(b, 0).abs().max()) for b in range(B))
     vmax = max(float(draw(b, 1).abs().max()) for b in range(B))
-    ks = kmax / E4M3_MAX
-    vs = vmax / E4M3_MAX
+    ks = kmax / FMT_MAX[kv_format]
+    vs = vmax / FMT_MAX[kv_format]
     for b in range(B):
         ids = phys_of[b]
-        k_cache[ids] = quantize_e4m3(draw(b, 0), ks).view(nmb, P, Hkv, D)
-        v_cache[ids] = quantize_e4m3(draw(b, 1), vs).view(nmb, P, Hkv, D)
+        k_cache[ids] = quantize_fp8(draw(b, 0), ks, kv_format).view(nmb, P, Hkv, D)
+        v_cache[ids] = quantize_fp8(draw(b, 1), vs, kv_format).view(nmb, P, Hkv, D)
         # tokens past the context in the last microblock are poisoned
         tail = nmb * P - L
         if tail:
@@ -360,6 +374,7 @@ def make_sparse(
         meta={"L": L, "topk_blocks": topk_blocks, "seed": seed,
               # logical microblock -> physical microblock of every request
               "block_table": phys_of.to(torch.int32)},
+        kv_format=kv_format,
     )
 
 
