@@ -768,6 +768,56 @@ def run_select_entries(args):
     }), flush=True)
 
 
+def run_small_reference(args, op):
+    """The oracle's merge or planner on the same shapes as the GPU lines,
+    whole calls, timed on the host (one thread)."""
+    _, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    if op == "dcp_merge":
+        n, D, R = 64 * 32, 128, 2
+        rng = np.random.default_rng(3)
+        outs = rng.standard_normal((R, n, D))
+        lses = rng.standard_normal((R, n)) * 4
+
+        def call():
+            oracle.merge(outs, lses)
+        metric, unit, alg = DCP_METRIC, "GB/s", R * n * (D + 1) * 4 + n * D * 2
+    else:
+        from synth import make_selection
+
+        Bn, q, topk, L = 4, 4, 2048, 131072
+        sel = make_selection(Bn, q, L, topk, seed=5).numpy()
+        bt = np.random.default_rng(1).permutation(Bn * (L // 4)).astype(np.int32).reshape(Bn, L // 4)
+
+        def call():
+            oracle.select_to_entries(sel, bt, L // 4, 0)
+        metric, unit, alg = SEL_METRIC, "us", None
+    for _ in range(max(1, min(args.warmup, 3))):
+        call()
+    t0 = time.time()
+    k = 0
+    while k < max(1, min(args.steps, 50)) and (k == 0 or time.time() - t0 < args.ref_budget / 4):
+        call()
+        k += 1
+    dt = (time.time() - t0) / k
+    value = round(alg / dt / 1e9, 5) if unit == "GB/s" else round(dt * 1e6, 1)
+    print(json.dumps({
+        "impl": "reference", "op": op, "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
+        "steps": k, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": unit == "GB/s", "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": f"{op}: the shapes of the GPU line"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": f"{k} whole call(s)"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -786,14 +836,12 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.op == "select_entries":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "op": "select_entries",
-                              "unavailable": "the planner is timed on the GPU only; its oracle is pinned in tests"}))
+            run_small_reference(args, "select_entries")
         else:
             run_select_entries(args)
     elif args.op == "dcp_merge":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "op": "dcp_merge",
-                              "unavailable": "the merge is timed on the GPU only; its oracle is pinned in tests"}))
+            run_small_reference(args, "dcp_merge")
         else:
             run_dcp_merge(args)
     elif args.op == "cache_write":
