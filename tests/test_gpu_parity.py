@@ -249,3 +249,14 @@ def test_tc_forced_splits(splits):
     dp = _dp(p, num_splits=splits, kernel=2)
     got = _run(dp)
     compare(got, _ref("c3_64k"), what=f"tc S={splits}", cond=_cond_if_long(dp, "c3_64k"))
+
+
+def test_oracle_decode_tables_match_cuda_conversions():
+    """The oracle's E4M3 and E5M2 tables against CUDA's own fp8 -> float
+    conversions on the device (a library call, all 256 codes)."""
+    codes = torch.arange(256, dtype=torch.uint8, device="cuda")
+    for table, dt in ((oracle.e4m3_table(), torch.float8_e4m3fn), (oracle.e5m2_table(), torch.float8_e5m2)):
+        dev = codes.view(dt).to(torch.float32).double().cpu().numpy()
+        assert np.array_equal(np.isnan(dev), np.isnan(table))
+        fin = ~np.isnan(table)
+        assert np.array_equal(dev[fin], table[fin])
