@@ -204,3 +204,64 @@ def test_select_to_entries_rejects_bad_arguments(B, bad):
 def test_select_to_entries_empty_batch(B):
     assert B.lib.fp8kv_attn_select_to_entries(None, None) == B.EINVAL
     assert B.lib.fp8kv_attn_select_to_entries(ctypes.byref(_sel(B, batch=0, sel=0, n_entries=0)), None) == B.OK
+
+
+# ------------------------------------------------------------------ merge / combine with LSE (host validation only)
+
+def _mg(B, **kw):
+    a = B.MergeArgs()
+    a.num_ranks, a.head_dim, a.num_vectors = 2, 128, 16
+    a.outs = a.lses = a.out = 0x10000  # never dereferenced: every call below is rejected
+    a.rank_stride_out, a.rank_stride_lse = 16 * 128, 16
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(num_ranks=0), dict(num_ranks=65), dict(head_dim=2), dict(head_dim=130), dict(head_dim=2048),
+    dict(num_vectors=-1), dict(outs=0), dict(outs=0x10008), dict(lses=0), dict(rank_stride_out=6),
+    dict(rank_stride_out=-4), dict(rank_stride_lse=-1), dict(out=0x10004), dict(out=0),
+])
+def test_merge_rejects_bad_arguments(B, bad):
+    assert B.lib.fp8kv_attn_merge(ctypes.byref(_mg(B, **bad)), None) == B.EINVAL
+
+
+@pytest.mark.parametrize("rank,kw", [(-1, {}), (2, {}), (0, {"out_f32": 0})])
+def test_merge_scale_rejects_bad_arguments(B, rank, kw):
+    a = _mg(B, out=0, out_f32=0x10000)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    assert B.lib.fp8kv_attn_merge_scale(ctypes.byref(a), rank, None) == B.EINVAL
+    # the scale step writes only out_f32
+    b = _mg(B, out=0x10000, out_f32=0x10000)
+    assert B.lib.fp8kv_attn_merge_scale(ctypes.byref(b), 0, None) == B.EINVAL
+
+
+def test_merge_with_nothing_to_do(B):
+    assert B.lib.fp8kv_attn_merge(None, None) == B.EINVAL
+    assert B.lib.fp8kv_attn_merge(ctypes.byref(_mg(B, num_vectors=0, outs=0, lses=0)), None) == B.OK
+
+
+def test_combine_lse_needs_its_outputs(B):
+    plan = B.fp8kv_attn_plan(_desc(B))
+    a = B.Args()
+    a.q = a.k_cache = a.v_cache = a.block_table = a.row_kv_len = 0x10000
+    a.workspace = 0x100000
+    a.workspace_bytes = plan.workspace_bytes
+    a.block_table_stride = 76
+    a.k_stride_block = a.v_stride_block = 1728 * 256
+    a.k_stride_token = a.v_stride_token = 256
+    a.k_stride_head = a.v_stride_head = 256
+    a.softmax_scale, a.k_scale, a.v_scale = 0.0625, 1.0, 1.0
+    vp = ctypes.c_void_p
+    assert B.lib.fp8kv_attn_combine_lse(ctypes.byref(plan), ctypes.byref(a), None, vp(0x10000), None) == B.EINVAL
+    assert B.lib.fp8kv_attn_combine_lse(ctypes.byref(plan), ctypes.byref(a), vp(0x10008), vp(0x10000), None) == B.EINVAL
+    assert B.lib.fp8kv_attn_combine_lse(ctypes.byref(plan), ctypes.byref(a), vp(0x10000), None, None) == B.EINVAL
+
+
+def test_plan_records_the_cache_format(B):
+    assert B.fp8kv_attn_plan(_desc(B)).kv_format == B.KV_E4M3
+    assert B.fp8kv_attn_plan(_desc(B, kv_format=B.KV_E5M2)).kv_format == B.KV_E5M2
+    with pytest.raises(B.Fp8kvError):
+        B.fp8kv_attn_plan(_desc(B, kv_format=2))
