@@ -15,7 +15,7 @@ from typing import Optional
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8kv_attn.so")
 
-REVISION = 2
+REVISION = 3
 OK = 0
 EINVAL = -1
 EUNSUPPORTED = -2
@@ -38,11 +38,14 @@ STATUS_BAD_LEN = 0x2
 STATUS_BAD_ENTRIES = 0x4
 STATUS_TIMEOUT = 0x8
 
+TEST_STALL_PIPELINE = 0x1
+
 
 class Desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "mode", "batch", "q_max", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
-        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits", "kernel", "kv_format")]
+        "max_kv_len", "max_blocks", "num_kv_blocks", "num_sms", "num_splits", "kernel", "kv_format",
+        "test_flags")]
 
 
 class Plan(ctypes.Structure):
@@ -56,7 +59,8 @@ class Plan(ctypes.Structure):
         ("partial_offset", ctypes.c_int64), ("ml_offset", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
         ("kv_format", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 15),
+        ("test_flags", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 14),
     ]
 
 
@@ -202,9 +206,10 @@ def fp8kv_attn_forward_static(plan: Plan, args: Args, stream: int = 0) -> None:
 def make_desc(*, mode: int, batch: int, q_max: int, num_q_heads: int, num_kv_heads: int,
               head_dim: int, page_size: int, max_kv_len: int, max_blocks: int,
               num_kv_blocks: int, num_sms: int = 0, num_splits: int = 0, kernel: int = 0,
-              kv_format: int = KV_E4M3) -> Desc:
+              kv_format: int = KV_E4M3, test_flags: int = 0) -> Desc:
     return Desc(mode, batch, q_max, num_q_heads, num_kv_heads, head_dim, page_size,
-                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits, kernel, kv_format)
+                max_kv_len, max_blocks, num_kv_blocks, num_sms, num_splits, kernel, kv_format,
+                test_flags)
 
 
 def _ptr(t) -> Optional[int]:

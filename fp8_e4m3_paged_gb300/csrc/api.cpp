@@ -48,6 +48,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   if (d->kernel < FP8KV_KERNEL_AUTO || d->kernel > FP8KV_KERNEL_TC) return FP8KV_EINVAL;
   if (d->kernel == FP8KV_KERNEL_TC && d->head_dim != 128 && d->head_dim != 256) return FP8KV_EUNSUPPORTED;
   if (d->kv_format != FP8KV_KV_E4M3 && d->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
+  if (d->test_flags & ~FP8KV_TEST_STALL_PIPELINE) return FP8KV_EINVAL;
   if (d->mode == FP8KV_MODE_DENSE) {
     if ((int64_t)d->max_blocks * d->page_size < d->max_kv_len) return FP8KV_EINVAL;
   } else {
@@ -80,6 +81,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   P.rows = d->q_max * P.group;
   P.num_sms = sms;
   P.kv_format = d->kv_format;
+  P.test_flags = d->test_flags;
 
   // Kernel choice: the tcgen05 path when the grouped rows fill at least a
   // quarter of its 64-row MMA tile and D is 128 or 256; otherwise the generic
@@ -104,6 +106,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
     ctas_per_sm = 2;
     max_part_tiles = kGenericMaxPartTiles;
   }
+  if (P.test_flags && P.kernel != kTc) return FP8KV_EINVAL;  // the switch targets the pipeline waits
   const int n_chunks = ceil_div(P.rows, P.row_chunk);
   P.tile_tokens = tile;
 
@@ -159,6 +162,7 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->max_blocks = plan->max_blocks;
   p->num_kv_blocks = plan->num_kv_blocks;
   p->kv_format = plan->kv_format;
+  p->test_flags = plan->test_flags;
   if (p->kv_format != FP8KV_KV_E4M3 && p->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
   if (p->G < 1 || p->rows != p->q_max * p->G || p->S < 1 || p->row_chunk < 1) return FP8KV_EINVAL;
 

@@ -39,20 +39,23 @@ __device__ __forceinline__ void e5m2x4_to_f32(uint32_t w, float (&o)[4]) {
   }
 }
 
-// Exact E4M3 -> fp16 pair for two bytes: result halves hold dec(b) * 2^-8.
-// With the byte in bits 8..15 of a 16-bit lane (h = b << 8), the fp16 pattern
-// is sign(h) | ((h >> 1) & 0x3F80): exponent bits eeee become the low four
-// bits of the fp16 exponent (bias 15 vs 7: a factor 2^-8) and mmm the top of
-// the fp16 mantissa; subnormals map to fp16 subnormals exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_lo(uint32_t w) {
-  // bytes 0,1 of w -> halves 0,1
-  const uint32_t h = __byte_perm(w, 0u, 0x1404u);  // [b1,0,b0,0] as bytes 3..0
-  return (h & 0x80008000u) | ((h >> 1) & 0x3F803F80u);
+// Byte lanes of the 16 cache bytes in w that hold a non-finite code, as the
+// top bit of each byte of the four words OR-ed together (0: all finite).
+// E4M3: 0x7F / 0xFF (NaN); E5M2: exponent field all ones (infinity or NaN).
+// For b' = b & 0x7F (E4M3) or b & 0x7C (E5M2), b' + 1 (+ 4) carries into bit
+// 7 exactly when b' is the all-ones pattern, and never into the next byte.
+__device__ __forceinline__ uint32_t nonfinite_codes(const uint4& w, bool e5m2) {
+  const uint32_t m = e5m2 ? 0x7C7C7C7Cu : 0x7F7F7F7Fu;
+  const uint32_t a = e5m2 ? 0x04040404u : 0x01010101u;
+  return (((w.x & m) + a) | ((w.y & m) + a) | ((w.z & m) + a) | ((w.w & m) + a)) & 0x80808080u;
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_hi(uint32_t w) {
-  // bytes 2,3 of w -> halves 0,1
-  const uint32_t h = __byte_perm(w, 0u, 0x3424u);
-  return (h & 0x80008000u) | ((h >> 1) & 0x3F803F80u);
+
+// The four bytes of x with every non-finite code replaced by 0.
+__device__ __forceinline__ uint32_t zap_nonfinite(uint32_t x, bool e5m2) {
+  const uint32_t m = e5m2 ? 0x7C7C7C7Cu : 0x7F7F7F7Fu;
+  const uint32_t a = e5m2 ? 0x04040404u : 0x01010101u;
+  const uint32_t top = ((x & m) + a) & 0x80808080u;  // bit 7 of each non-finite byte
+  return x & ~((top >> 7) * 0xFFu);
 }
 
 __device__ __forceinline__ void set_status(unsigned int* status, unsigned int bit) {

@@ -27,6 +27,7 @@ struct Params {
   int32_t mode, B, q_max, Hq, Hkv, D, G, rows, row_chunk, n_row_chunks, S;
   int32_t page_size, max_kv_len, max_blocks, num_kv_blocks;
   int32_t kv_format;  // FP8KV_KV_E4M3 or FP8KV_KV_E5M2
+  int32_t test_flags; // FP8KV_TEST_* (0 in production)
   // inputs
   const uint16_t* q;
   const uint8_t* k_cache;

@@ -11,8 +11,11 @@
 // and finally stores the unnormalised FP32 numerators acc with (m, l)
 // ("DFlash2 E4M3 attention with FP32 state", intro paragraph 4: FP32
 // partition numerators, separate FP32 max/sum).  Masked tokens get s = -inf by
-// selection, so their p is exactly 0 and their V values (finite by
-// construction of the decode, zero-filled when not loaded) add exactly 0.
+// selection and p = -0.0 (a visible token whose weight underflows gets +0.0).
+// A tile whose V bytes hold no non-finite code takes the plain FMA loop (a
+// masked token's -0.0 * v then adds nothing); a tile with a NaN (or E5M2
+// infinity) code in V skips the tokens each row does not see, so the code
+// reaches exactly the rows that see its token, as in the exact softmax.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
   __syncthreads();
 
   for (int tb = u0; tb < u1; tb += unit) {
+    bool vbad = false;  // this thread loaded a non-finite V code
     // ------------------------------------------------------ load + decode
     // 16-byte vectors: TT tokens x D/16 vectors for K and for V.
     constexpr int VPT = D / 16;
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
       const uint32_t kwa[4] = {kw.x, kw.y, kw.z, kw.w};
       const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
       const bool e5 = p.kv_format == FP8KV_KV_E5M2;  // uniform
+      vbad |= nonfinite_codes(vw, e5) != 0u;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (e5)
@@ -218,7 +223,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
         *reinterpret_cast<float4*>(&Vs[t * D + vv * 16 + j * 4]) = make_float4(f[0], f[1], f[2], f[3]);
       }
     }
-    __syncthreads();
+    const bool vflag = __syncthreads_or(vbad) != 0;  // the tile holds a non-finite V code
 
     // ------------------------------------------------------ scores (lane = token)
     // Compensated QK: products q*k are exact in FP32 (11-bit x 4-bit
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
         const float m_new = fmaxf(m_run[k], ceilf(mt));
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float arg = fmaf(lo[k], c, fmaf(hi[k], c, -m_use));
-        const float pv = vis ? exp2f(arg) : 0.f;
+        const float pv = vis ? exp2f(arg) : -0.f;  // -0.0 marks "not seen"
         const float alpha = (m_run[k] == -INFINITY) ? 0.f : exp2_int(m_run[k] - m_use);
         float ps = pv;
 #pragma unroll
@@ -292,18 +297,38 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
           acc[k].x *= a; acc[k].y *= a; acc[k].z *= a; acc[k].w *= a;
         }
       }
+      if (!vflag) {
 #pragma unroll 4
-      for (int t = 0; t < TT; ++t) {
-        const float4 v4 = *reinterpret_cast<const float4*>(&Vs[t * D + dg * 4]);
+        for (int t = 0; t < TT; ++t) {
+          const float4 v4 = *reinterpret_cast<const float4*>(&Vs[t * D + dg * 4]);
 #pragma unroll
-        for (int k = 0; k < RPT; ++k) {
-          const int i = rg + k * RG;
-          if (i < RCMAX) {
-            const float pv = Ps[t * (RCMAX + 1) + i];
-            acc[k].x = fmaf(pv, v4.x, acc[k].x);
-            acc[k].y = fmaf(pv, v4.y, acc[k].y);
-            acc[k].z = fmaf(pv, v4.z, acc[k].z);
-            acc[k].w = fmaf(pv, v4.w, acc[k].w);
+          for (int k = 0; k < RPT; ++k) {
+            const int i = rg + k * RG;
+            if (i < RCMAX) {
+              const float pv = Ps[t * (RCMAX + 1) + i];
+              acc[k].x = fmaf(pv, v4.x, acc[k].x);
+              acc[k].y = fmaf(pv, v4.y, acc[k].y);
+              acc[k].z = fmaf(pv, v4.z, acc[k].z);
+              acc[k].w = fmaf(pv, v4.w, acc[k].w);
+            }
+          }
+        }
+      } else {
+        // a NaN or infinite V value only reaches the rows that see its token
+        for (int t = 0; t < TT; ++t) {
+          const float4 v4 = *reinterpret_cast<const float4*>(&Vs[t * D + dg * 4]);
+#pragma unroll
+          for (int k = 0; k < RPT; ++k) {
+            const int i = rg + k * RG;
+            if (i < RCMAX) {
+              const float pv = Ps[t * (RCMAX + 1) + i];
+              if (__float_as_uint(pv) != 0x80000000u) {
+                acc[k].x = fmaf(pv, v4.x, acc[k].x);
+                acc[k].y = fmaf(pv, v4.y, acc[k].y);
+                acc[k].z = fmaf(pv, v4.z, acc[k].z);
+                acc[k].w = fmaf(pv, v4.w, acc[k].w);
+              }
+            }
           }
         }
       }

@@ -49,8 +49,20 @@
 // tile exceeds it by more than kTau, so P <= 2^kTau always fits fp16 and the
 // rescale factor of O is an exact power of two.
 //
-// Every wait is bounded; a wait that gives up sets FP8KV_STATUS_TIMEOUT and
-// the kernel finishes without hanging (results are then invalid).
+// Every wait is bounded.  A wait that gives up sets a CTA-wide abort flag and
+// FP8KV_STATUS_TIMEOUT; every role then stops issuing work, the producers wait
+// for the bulk copies they already issued and the MMA thread for the UMMAs it
+// already committed (both always complete), and only then is TMEM freed and
+// the CTA allowed to exit (results of that launch are invalid).
+//
+// Non-finite V codes (E4M3 NaN, E5M2 infinities and NaNs): the P.V product
+// runs over every token a tile copied, including tokens some rows do not see
+// (their P is exactly 0), and 0 * NaN would reach those rows.  The V decoders
+// therefore write such codes as 0 and flag the CTA; after the main loop a
+// flagged CTA re-reads its partition's V bytes and sets the numerator element
+// (vector, column) to NaN or +-infinity for exactly the vectors that see the
+// token, as the exact softmax has it.  Unflagged CTAs (the normal case) only
+// pay the byte test in the V decoders.
 #include <cstdint>
 
 #include <cuda_fp16.h>
@@ -78,7 +90,9 @@ constexpr int kProdWarp = kMmaWarp + 1;                // 13 (K), 14 (V)
 constexpr int kThreads = 32 * (kProdWarp + 2);        // 480
 static_assert(kThreads == kTcThreads && kT == kTcTileTokens, "launch shape");
 constexpr float kTau = 8.0f;        // lazy-rescale threshold (base-2 units)
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimit = 1u << 20;      // polls per wait (product path)
+constexpr uint32_t kTestWaitLimit = 1u << 12;  // polls per wait under FP8KV_TEST_STALL_PIPELINE
+constexpr uint32_t kDrainLimit = 1u << 20;     // polls for issued copies / UMMAs to complete
 constexpr int kMaxStages = 4;
 constexpr int kSBuf = 4;            // S/P buffers in TMEM
 
@@ -121,6 +135,9 @@ struct Meta {
   uint64_t validv[kMaxStages];          // the same for the raw V stage
   uint32_t pmask[2][kE];                // sparse: entry masks of the tile each stream copies
   int32_t nrow[kRows];                  // dense: live length of each query vector; sparse: its query row
+  uint64_t drain;                       // the MMA thread's final commit (all its UMMAs done)
+  uint32_t abort;                       // a wait gave up: every role stops
+  uint32_t vbad;                        // a V decoder met a non-finite code
 };
 static_assert(sizeof(Meta) <= 1024, "meta block");
 
@@ -234,9 +251,10 @@ __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
 // lt / (D/16) + k * R (R = rows per pass of all threads), so every address
 // is a per-thread base plus a compile-time offset; all loads are issued
 // before the first conversion.  Rows whose bit in `valid` is clear were not
-// copied and become zeros.
-template <int D, int DBS, int FMT>
-__device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uint64_t valid, int lt) {
+// copied and become zeros.  With CHECK (the V stream) a non-finite code is
+// written as 0 and `bad` is set (see the kernel's header).
+template <int D, int DBS, int FMT, bool CHECK>
+__device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uint64_t valid, int lt, bool& bad) {
   constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
   constexpr int kR = kDecThreads / kChunks; // rows per pass
   constexpr int kPer = kT / kR;             // chunks per thread
@@ -257,6 +275,18 @@ __device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uin
   for (int k = 0; k < kPer; ++k) {
     w[k] = (full || ((valid >> (t0 + k * kR)) & 1ull)) ? *reinterpret_cast<const uint4*>(src + k * kR * D)
                                                       : make_uint4(0, 0, 0, 0);
+  }
+  if (CHECK) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if (nonfinite_codes(w[k], FMT == FP8KV_KV_E5M2) != 0u) {
+        bad = true;
+        w[k].x = zap_nonfinite(w[k].x, FMT == FP8KV_KV_E5M2);
+        w[k].y = zap_nonfinite(w[k].y, FMT == FP8KV_KV_E5M2);
+        w[k].z = zap_nonfinite(w[k].z, FMT == FP8KV_KV_E5M2);
+        w[k].w = zap_nonfinite(w[k].w, FMT == FP8KV_KV_E5M2);
+      }
+    }
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
@@ -318,6 +348,70 @@ __device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* ca
     }
   }
   return valid;
+}
+
+// A CTA whose V decoders met a non-finite code (written as 0 in the operand)
+// restores its effect on the partial numerators: every thread of the CTA
+// re-reads the V bytes of the partition's tokens (the copied ones: dense all
+// tokens below the longest row, sparse the tokens some row sees), and for
+// each non-finite byte (token t, column d) marks every query vector i that
+// sees t; then element (i, d) of the numerator becomes NaN (a NaN code, or
+// infinities of both signs) or +-infinity.  `scratch` holds one byte per
+// (vector, column): bit 0 NaN, bit 1 +inf, bit 2 -inf.
+template <int D, int MODE, int FMT>
+__device__ __noinline__ void patch_nonfinite_v(const Params& p, uint8_t* scratch, const int32_t* nrow, int b, int g,
+                                               int u0, int u1, int RC, int64_t prow) {
+  constexpr int kC = D / 16;  // 16-byte chunks per row
+  uint32_t* kinds = reinterpret_cast<uint32_t*>(scratch);
+  const int tid = threadIdx.x;
+  for (int x = tid; x < kRows * D / 4; x += kThreads) kinds[x] = 0u;
+  __syncthreads();
+  const bool e5 = FMT == FP8KV_KV_E5M2;
+  const int n_tok = (MODE == FP8KV_MODE_DENSE) ? (u1 - u0) : 4 * (u1 - u0);
+  for (int x = tid; x < n_tok * kC; x += kThreads) {
+    const int tu = x / kC, c = x % kC;
+    const uint8_t* row;
+    int tok = 0, tk = 0;
+    uint32_t mk = 0u;
+    if (MODE == FP8KV_MODE_DENSE) {
+      tok = u0 + tu;
+      const int blk = p.block_table[(int64_t)b * p.bt_stride + tok / p.page_size];
+      if (blk < 0 || blk >= p.num_kv_blocks) continue;
+      row = p.v_cache + blk * p.vsb + (tok % p.page_size) * p.vst + g * p.vsh;
+    } else {
+      const int e = u0 + tu / 4;
+      tk = tu % 4;
+      mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
+      const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
+      if ((mk & (0x11111111u << tk)) == 0u || blk < 0 || blk >= p.num_kv_blocks) continue;
+      row = p.v_cache + blk * p.vsb + tk * p.vst + g * p.vsh;
+    }
+    const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+    if (nonfinite_codes(w, e5) == 0u) continue;
+    const uint32_t wa[4] = {w.x, w.y, w.z, w.w};
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t byte = (wa[j / 4] >> (8 * (j % 4))) & 0xFFu;
+      const bool nf = e5 ? ((byte & 0x7Cu) == 0x7Cu) : ((byte & 0x7Fu) == 0x7Fu);
+      if (!nf) continue;
+      // E4M3: NaN; E5M2: mantissa bits set -> NaN, else an infinity of the byte's sign
+      const uint32_t kind = (!e5 || (byte & 0x3u)) ? 1u : ((byte & 0x80u) ? 4u : 2u);
+      const int d = c * 16 + j;
+      for (int i = 0; i < RC; ++i) {
+        const int n = nrow[i];
+        const bool sees = (MODE == FP8KV_MODE_DENSE) ? (tok < n) : (n >= 0 && ((mk >> (4 * n + tk)) & 1u));
+        if (sees) atomicOr(&kinds[i * (D / 4) + d / 4], kind << (8 * (d % 4)));
+      }
+    }
+  }
+  __syncthreads();
+  for (int x = tid; x < RC * D; x += kThreads) {
+    const int i = x / D, d = x % D;
+    const uint32_t k = (kinds[i * (D / 4) + d / 4] >> (8 * (d % 4))) & 0xFFu;
+    if (k == 0u) continue;
+    const float v = ((k & 1u) || (k & 6u) == 6u) ? __uint_as_float(0x7FC00000u)
+                                                  : ((k & 2u) ? INFINITY : -INFINITY);
+    p.partial[(prow + i) * D + d] = v;
+  }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -418,6 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       mbar_init(&mt.pv_done[i], 1);
       mbar_init(&mt.p_ready[i], 2 * 32 * kSoftmaxWarps);
     }
+    mbar_init(&mt.drain, 1);
+    mt.abort = 0u;
+    mt.vbad = 0u;
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -442,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = mt.tmem;
+  volatile uint32_t* const abort_flag = &mt.abort;
+  const uint32_t wlim = (p.test_flags & FP8KV_TEST_STALL_PIPELINE) ? kTestWaitLimit : kWaitLimit;
 
   if (warp == kProdWarp || warp == kProdWarp + 1) {
     // ======================================================== producers
@@ -455,7 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
       uint32_t* masks = mt.pmask[is_k ? 0 : 1];
       bool ok = true;
-      for (int i = 0; i < n_tiles; ++i) {
+      int issued = 0;  // tiles whose copies were issued
+      for (int i = 0; i < n_tiles && ok; ++i) {
         const int slot = i % C::kRaw;
         if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
           // entry masks of the tile (all loads first); an entry with a bad
@@ -476,19 +576,37 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
             }
           }
           // the masks are read only by this thread, after the stage is free
-          if (i >= C::kRaw) {
-            if (!mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, kWaitLimit)) ok = false;
+          if (i >= C::kRaw && !mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag)) {
+            ok = false;
+            break;
           }
 #pragma unroll
           for (int el = 0; el < kE; ++el) masks[el] = mk[el];
         } else if (i >= C::kRaw) {
           // the raw stage is free once the decoders took its previous tile
-          if (!mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, kWaitLimit)) ok = false;
+          if (!mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag)) {
+            ok = false;
+            break;
+          }
         }
         valid[slot] = copy_rows<D, MODE>(p, cache, csb, cst, csh, b, g, u0, u1, i,
                                          raw_base + slot * C::kRawBytes, &raw_full[slot], masks, is_k);
+        issued = i + 1;
+        if (is_k && i == 0 && (p.test_flags & FP8KV_TEST_STALL_PIPELINE)) {
+          // test only: hold back this arrival until a waiting warp has given
+          // up, so that the timeout path runs; then stop issuing
+          for (uint32_t k = 0; k < kDrainLimit && *abort_flag == 0u; ++k) __nanosleep(256);
+          mbar_arrive(&raw_full[slot]);
+          break;
+        }
         mbar_arrive(&raw_full[slot]);
       }
+      // Drain: the copies of the last tile of every stage must have landed
+      // before the CTA may exit (the decoders normally consumed them already;
+      // after a give-up they may not have).  Nobody else arms these barriers,
+      // so each last phase completes once its bytes arrive.
+      for (int i = max(0, issued - C::kRaw); i < issued; ++i)
+        mbar_wait_plain(&raw_full[i % C::kRaw], (i / C::kRaw) & 1, kDrainLimit);
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -504,29 +622,32 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     const uint64_t* valid = is_k ? mt.validk : mt.validv;
     const uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
     uint8_t* op_base = smem + (is_k ? C::kOffK : C::kOffV);
-    bool ok = true;
+    bool ok = true, bad = false;
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i % C::kRaw;
       const int st = i % n_stages;
       // raw rows arrived, and the operand stage is free (the MMA that read
       // its previous tile, and that tile's partner, is done)
-      if (!mbar_wait(&raw_full[slot], (i / C::kRaw) & 1, kWaitLimit)) ok = false;
-      if (i >= n_stages) {
-        if (!mbar_wait(&op_empty[st / 2], ((i / n_stages) - 1) & 1, kWaitLimit)) ok = false;
+      if (!mbar_wait(&raw_full[slot], (i / C::kRaw) & 1, wlim, abort_flag) ||
+          (i >= n_stages && !mbar_wait(&op_empty[st / 2], ((i / n_stages) - 1) & 1, wlim, abort_flag))) {
+        ok = false;
+        break;
       }
       if (is_k) {
         // K stages hold pairs of tiles interleaved per column block, so that
         // two consecutive tiles form one 128-row operand of the pair's QK
         uint8_t* op = op_base + (st / 2) * (2 * C::kOpBytes) + (st % 2) * (kT * 128);
-        decode_tile<D, 2 * kT * 128, FMT>(raw_base + slot * C::kRawBytes, op, valid[slot], lt);
+        decode_tile<D, 2 * kT * 128, FMT, false>(raw_base + slot * C::kRawBytes, op, valid[slot], lt, bad);
       } else {
-        decode_tile<D, kT * 128, FMT>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes, valid[slot], lt);
+        decode_tile<D, kT * 128, FMT, true>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes,
+                                            valid[slot], lt, bad);
       }
       fence_proxy_async_smem();
       mbar_arrive(&op_full[st / 2]);
       if ((i & 1) == 0 && i + 1 == n_tiles) mbar_arrive(&op_full[st / 2]);  // a last tile without partner
       mbar_arrive(&raw_empty[slot]);
     }
+    if (bad) mt.vbad = 1u;
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
@@ -549,8 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         const int i0 = 2 * m;
         const bool two = i0 + 1 < n_tiles;
         const int st0 = i0 % C::kKStages;
-        if (!mbar_wait(&mt.k_full[st0 / 2], (i0 / C::kKStages) & 1, kWaitLimit)) ok = false;
-        if (m >= 2 && !mbar_wait(&mt.pv_done[m & 1], ((m >> 1) - 1) & 1, kWaitLimit)) ok = false;
+        if (!mbar_wait(&mt.k_full[st0 / 2], (i0 / C::kKStages) & 1, wlim, abort_flag) ||
+            (m >= 2 && !mbar_wait(&mt.pv_done[m & 1], ((m >> 1) - 1) & 1, wlim, abort_flag))) {
+          ok = false;
+          return;
+        }
         tc_fence_after();
         const uint32_t sk = smem_u32(smem + C::kOffK + (st0 / 2) * (2 * C::kOpBytes));
         const uint32_t idesc = two ? idesc_qk2 : idesc_qk;
@@ -567,8 +691,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       auto issue_pv = [&](int m) {
         const int j0 = 2 * m;
         const int sv0 = j0 % C::kVStages;
-        if (!mbar_wait(&mt.p_ready[m & 1], (m >> 1) & 1, kWaitLimit)) ok = false;
-        if (!mbar_wait(&mt.v_full[sv0 / 2], (j0 / C::kVStages) & 1, kWaitLimit)) ok = false;
+        if (!mbar_wait(&mt.p_ready[m & 1], (m >> 1) & 1, wlim, abort_flag) ||
+            !mbar_wait(&mt.v_full[sv0 / 2], (j0 / C::kVStages) & 1, wlim, abort_flag)) {
+          ok = false;
+          return;
+        }
         tc_fence_after();
         for (int j = j0; j < j0 + 2 && j < n_tiles; ++j) {
           const uint32_t sv = smem_u32(smem + C::kOffV + (j % C::kVStages) * C::kOpBytes);
@@ -587,6 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         if (m + 1 < n_pairs) issue_qk(m + 1);
         if (ok) issue_pv(m);
       }
+      // Drain: every UMMA this thread issued must be done before TMEM is
+      // freed (normally the softmax warps already waited for the last PVs).
+      mma_commit(&mt.drain);
+      mbar_wait_plain(&mt.drain, 0, kDrainLimit);
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -602,8 +733,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     const int n_a = mt.nrow[ra], n_b = mt.nrow[rb];
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      if (!mbar_wait(&mt.s_full[(i >> 1) & 1], (i >> 2) & 1, kWaitLimit)) ok = false;
+    for (int i = 0; i < n_tiles && ok; ++i) {
+      if (!mbar_wait(&mt.s_full[(i >> 1) & 1], (i >> 2) & 1, wlim, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       if (warp_live) {
         uint32_t sr[32];
@@ -721,8 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
           // pair once their PVs are done, and for an odd tile the partner's P,
           // made under the previous max, has not gone through its PV yet.
           const int m = i >> 1;
-          if (m >= 1) {
-            if (!mbar_wait(&mt.pv_done[(m - 1) & 1], ((m - 1) >> 1) & 1, kWaitLimit)) ok = false;
+          if (m >= 1 && mbar_wait(&mt.pv_done[(m - 1) & 1], ((m - 1) >> 1) & 1, wlim, abort_flag)) {
             tc_fence_after();
             // thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16 (the
             // P_hi row for lane < 16, its P_lo twin above); the alpha of vector
@@ -761,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     }
     // ------------------------------------------------------ epilogue
     const int last_pair = (n_tiles - 1) >> 1;
-    if (!mbar_wait(&mt.pv_done[last_pair & 1], (last_pair >> 1) & 1, kWaitLimit)) ok = false;
+    if (!ok || !mbar_wait(&mt.pv_done[last_pair & 1], (last_pair >> 1) & 1, wlim, abort_flag)) ok = false;
     tc_fence_after();
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     if (warp_live) {
@@ -801,6 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (mt.vbad) patch_nonfinite_v<D, MODE, FMT>(p, smem + C::kOffRawK, mt.nrow, b, g, u0, u1, RC, prow);
 }
 
 template <int D, int MODE, int FMT>

@@ -11,9 +11,11 @@
 // Host code cannot use the array's name as a device address; its address is
 // looked up once per device with cudaGetSymbolAddress (with that device
 // current) on the first call made on that device.  That first call should
-// therefore happen before any stream capture.  Every call shares the one
-// array: calls whose kernels overlap on the GPU (different streams, or two
-// host threads) race on it and must be serialised by the caller.
+// therefore happen before any stream capture.  The address is cached for the
+// life of the process, so a device reset (cudaDeviceReset) between calls is
+// not supported.  Every call shares the one array: calls whose kernels overlap
+// on the GPU (different streams, or two host threads) race on it and must be
+// serialised by the caller.
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -67,8 +69,13 @@ extern "C" int fp8kv_attn_forward_static(const fp8kv_attn_plan_t* plan, const fp
   Params p;
   int rc = build_params(plan, &s, &p);
   if (rc != FP8KV_OK) return rc;
-  if (p.B == 0) return FP8KV_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (p.B == 0) {
+    // nothing to run; a caller's status word still reads "no anomaly"
+    if (a->workspace && a->workspace_bytes >= 4 && cudaMemsetAsync(a->workspace, 0, 4, st) != cudaSuccess)
+      return FP8KV_ECUDA;
+    return FP8KV_OK;
+  }
   // The array keeps the previous call's contents: the sticky status word
   // must start at zero; every partial the combine reads is rewritten first.
   if (cudaMemsetAsync(scratch, 0, 4, st) != cudaSuccess) return FP8KV_ECUDA;

@@ -38,31 +38,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe of a phase.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait: returns false after `limit` unsuccessful polls (each poll may
 // itself block for a hardware-defined interval), so that no wait can hang.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
+// `abort` is a CTA-wide flag in shared memory: the first wait that gives up
+// sets it, and every later wait of any warp that finds it set returns false
+// at once instead of spending its own full budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit,
+                                          volatile uint32_t* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 1; i < limit; ++i) {
+    if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
+  }
+  *abort = 1u;
   return false;
 }
 
-// Arrive and add `tx` expected transaction bytes to the current phase.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(tx)
-               : "memory");
+// Bounded wait that ignores the abort flag: for work already issued (bulk
+// copies, UMMAs), which always completes; returns false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait_plain(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 // Add `tx` expected transaction bytes to the current phase (no arrival).
@@ -81,21 +78,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
       : "memory");
 }
 
-// Release store / acquire load of a 32-bit word in shared memory (a flag one
-// thread publishes and another polls).
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-// Relaxed store (a counter whose readers need no ordering with earlier work).
-__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.relaxed.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -106,25 +88,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Named barrier over a subset of warps (id 1..15, count a multiple of 32).
-// bar.sync is the aligned form: every lane of a participating warp must
-// execute it together (reconverge with __syncwarp after lane-divergent code).
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return out != 0;
 }
 
 // ------------------------------------------------------------------ TMEM
@@ -185,7 +148,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ UMMA
 

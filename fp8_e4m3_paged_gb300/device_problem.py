@@ -18,7 +18,7 @@ from . import binding as B
 class DeviceProblem:
     def __init__(self, p, *, device: str = "cuda", num_splits: int = 0, num_sms: int = 0,
                  kv_copies: int = 1, device_scales: bool = False, k_cache=None, v_cache=None,
-                 kernel: int = 0):
+                 kernel: int = 0, test_flags: int = 0):
         self.p = p
         dev = torch.device(device)
         self.q = p.q_fp16.to(dev).contiguous()
@@ -46,7 +46,7 @@ class DeviceProblem:
         self.desc = B.make_desc(
             mode=mode, batch=p.B, q_max=p.q, num_q_heads=p.Hq, num_kv_heads=p.Hkv,
             head_dim=p.D, page_size=p.page_size, max_kv_len=max_kv_len, max_blocks=max_blocks,
-            num_kv_blocks=int(kc.shape[0]), num_sms=num_sms, num_splits=num_splits, kernel=kernel,
+            num_kv_blocks=int(kc.shape[0]), num_sms=num_sms, num_splits=num_splits, kernel=kernel, test_flags=test_flags,
             kv_format=B.KV_E5M2 if getattr(p, "kv_format", "e4m3") == "e5m2" else B.KV_E4M3)
         self.plan = B.fp8kv_attn_plan(self.desc)
         self.workspace = torch.zeros(int(self.plan.workspace_bytes), dtype=torch.uint8, device=dev)

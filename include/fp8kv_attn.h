@@ -69,7 +69,7 @@ extern "C" {
  * stale plan cannot reach kernels with another partial layout ("DFlash2 E4M3
  * attention with FP32 state", intro paragraph 5: the wrapper requires a given
  * precision capability revision). */
-#define FP8KV_ATTN_REVISION 2
+#define FP8KV_ATTN_REVISION 3
 
 /* Return codes. */
 #define FP8KV_OK 0
@@ -99,7 +99,15 @@ extern "C" {
 #define FP8KV_STATUS_BAD_BLOCK 0x1   /* block / microblock id outside [0, num_kv_blocks) */
 #define FP8KV_STATUS_BAD_LEN 0x2     /* a row length < 0 or > max_kv_len (clamped) */
 #define FP8KV_STATUS_BAD_ENTRIES 0x4 /* n_entries < 0 or > max_blocks (clamped) */
-#define FP8KV_STATUS_TIMEOUT 0x8     /* a bounded pipeline wait gave up */
+#define FP8KV_STATUS_TIMEOUT 0x8     /* a bounded pipeline wait gave up (results invalid) */
+
+/* Test-only switches (desc.test_flags; 0 in production).
+ * FP8KV_TEST_STALL_PIPELINE: the tensor-core split kernel's K producer holds
+ * back its first arrival until another warp's bounded wait has given up, and
+ * waits use a short poll budget, so that the give-up path (abort, drain of
+ * issued copies and UMMAs, FP8KV_STATUS_TIMEOUT) runs on purpose.  Accepted
+ * only with the tensor-core kernel; the launch's results are invalid. */
+#define FP8KV_TEST_STALL_PIPELINE 0x1
 
 /* cudaStream_t without including CUDA headers (same type). */
 typedef struct CUstream_st* fp8kv_stream_t;
@@ -121,6 +129,7 @@ typedef struct {
   int32_t num_splits;    /* split-KV partitions per (request, KV head); 0 = planner's choice */
   int32_t kernel;        /* FP8KV_KERNEL_*: 0 = planner's choice */
   int32_t kv_format;     /* FP8KV_KV_*: 0 = E4M3 */
+  int32_t test_flags;    /* FP8KV_TEST_*: 0 in production */
 } fp8kv_attn_desc;
 
 /* A plan: plain data, owned by the caller, nothing to free.  Fields other than
@@ -143,7 +152,8 @@ typedef struct {
   int64_t ml_offset;       /* byte offset of FP32 (max, sum) pairs */
   int64_t workspace_bytes; /* minimum workspace size */
   int32_t kv_format;       /* FP8KV_KV_* of the cache bytes */
-  int32_t reserved[15];
+  int32_t test_flags;      /* FP8KV_TEST_* (0 in production) */
+  int32_t reserved[14];
 } fp8kv_attn_plan_t;
 
 /* Per-call arguments.  All pointers are device pointers owned by the caller,
@@ -339,8 +349,10 @@ int fp8kv_attn_select_to_entries(const fp8kv_select_args* a, fp8kv_stream_t stre
  * Nothing is allocated or freed.  `a` is used as for fp8kv_attn_split except
  * that a->workspace is not the scratch: if it is non-NULL and
  * a->workspace_bytes >= 4, the call's 32-bit status word is copied there (in
- * stream order) after the combine.  The first call on a device looks the
- * array's address up for that device; make it before any stream capture.
+ * stream order) after the combine (with batch 0, the word is set to 0).  The
+ * first call on a device looks the array's address up for that device; make
+ * it before any stream capture.  The address is kept for the life of the
+ * process: a device reset between calls is not supported.
  * Every call shares the one array: calls whose kernels may overlap on the GPU
  * (other streams, other host threads) race on it and must be serialised. */
 int fp8kv_attn_forward_static(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,

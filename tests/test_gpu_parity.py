@@ -109,8 +109,11 @@ def test_c4_full():
     assert dp.status() == 0
 
 
-def test_graph_replay_changing_lengths():
-    p = _problem("c3_64k")
+@pytest.mark.parametrize("name", ["c3_64k", "c3_128k", "c3_256k"])
+def test_graph_replay_changing_lengths(name):
+    """One graph captured at q_max = 8, replayed with 8, 5, 0 and 8 live rows
+    (the verify workload's three contexts); then 100 bitwise-equal replays."""
+    p = _problem(name)
     dp = _dp(p)
     L = p.max_kv_len
     s = torch.cuda.Stream()
@@ -128,7 +131,8 @@ def test_graph_replay_changing_lengths():
         torch.cuda.synchronize()
         got = dp.out.float().cpu().numpy()
         ref = oracle.attention(p, row_len=rl)
-        compare(got, ref, what=f"replay q_live={q_live}")
+        compare(got, ref, what=f"{name} replay q_live={q_live}")
+        assert dp.status() == 0
         if q_live == 0:
             assert np.all(got == 0.0) and not np.signbit(got).any()
     # bitwise determinism over repeated replays
@@ -260,3 +264,30 @@ def test_oracle_decode_tables_match_cuda_conversions():
         assert np.array_equal(np.isnan(dev), np.isnan(table))
         fin = ~np.isnan(table)
         assert np.array_equal(dev[fin], table[fin])
+
+
+def test_stalled_pipeline_gives_up_and_reports_timeout():
+    """The tensor-core kernel's bounded waits: with the test switch that holds
+    back the K producer's first arrival, a waiting warp gives up, every role
+    stops, issued copies and UMMAs drain, and the launch returns with
+    FP8KV_STATUS_TIMEOUT set.  The context stays usable: the same problem then
+    runs normally and matches the oracle."""
+    from fp8_e4m3_paged_gb300 import binding as B
+
+    p = _problem("c2")
+    dp = _dp(p, kernel=2, test_flags=B.TEST_STALL_PIPELINE)
+    dp.run()
+    torch.cuda.synchronize()
+    assert dp.status() & B.STATUS_TIMEOUT
+    good = _dp(p, kernel=2)
+    got = _run(good)
+    compare(got, _ref("c2"), what="c2 after a timed-out launch")
+    assert good.status() == 0
+
+
+def test_stall_switch_needs_the_tensor_core_kernel():
+    from fp8_e4m3_paged_gb300 import binding as B
+
+    with pytest.raises(B.Fp8kvError) as ei:
+        _dp(_problem("c1"), kernel=1, test_flags=B.TEST_STALL_PIPELINE)
+    assert ei.value.code == B.EINVAL
