@@ -13,6 +13,10 @@
 // combination, FP16 final activation; "Qwen4Exp: fp8_e4m3 main KV cache on
 // the QSA path", review: v_scale acts as the output scale).
 //
+// The weighted numerators are summed with TwoSum into a hi + lo pair (the
+// weights are powers of two, so each product is exact): an output that
+// cancels across partitions keeps the precision of its partials.
+//
 // One CTA per (query vector, 64-wide slice of D); its 256 threads are 16
 // partition lanes x 16 float4 columns.  The kernel is latency-bound (a few
 // MB in total), so the (m, l) pairs of all partitions and the numerators a
@@ -48,6 +52,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
   __shared__ float s_w[MAXS];       // weight 2^(m_s - M) of live partitions (0 = dead)
   __shared__ float s_l[MAXS];
   __shared__ float4 red_o[SL][DW / 4];
+  __shared__ float4 red_lo[SL][DW / 4];
   __shared__ float red_l[SL];
   const int D = p.D;
   const int n_slices = D / DW;
@@ -66,7 +71,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
 
   const int sl = tid / (DW / 4), c4 = tid % (DW / 4);
   const float* acc = p.partial + base * D + slice * DW + c4 * 4;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f), ol = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
   float M = -INFINITY;
   for (int s0 = 0; s0 < S; s0 += MAXS) {
@@ -129,10 +134,10 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
       const int k = sl + j * SL;
       const float w = (k < ns) ? s_w[k] : 0.f;
       if (w != 0.f) {
-        o.x = fmaf(w, a[j].x, o.x);
-        o.y = fmaf(w, a[j].y, o.y);
-        o.z = fmaf(w, a[j].z, o.z);
-        o.w = fmaf(w, a[j].w, o.w);
+        two_sum_acc(o.x, ol.x, w * a[j].x);
+        two_sum_acc(o.y, ol.y, w * a[j].y);
+        two_sum_acc(o.z, ol.z, w * a[j].z);
+        two_sum_acc(o.w, ol.w, w * a[j].w);
         L = fmaf(w, s_l[k], L);
       }
     }
@@ -151,30 +156,39 @@ __global__ void __launch_bounds__(CT) combine_kernel(Params p) {
       for (int j = 0; j < NB; ++j) {
         const int k = k0 + j * SL;
         if (w[j] != 0.f) {
-          o.x = fmaf(w[j], b4[j].x, o.x);
-          o.y = fmaf(w[j], b4[j].y, o.y);
-          o.z = fmaf(w[j], b4[j].z, o.z);
-          o.w = fmaf(w[j], b4[j].w, o.w);
+          two_sum_acc(o.x, ol.x, w[j] * b4[j].x);
+          two_sum_acc(o.y, ol.y, w[j] * b4[j].y);
+          two_sum_acc(o.z, ol.z, w[j] * b4[j].z);
+          two_sum_acc(o.w, ol.w, w[j] * b4[j].w);
           L = fmaf(w[j], s_l[k], L);
         }
       }
     }
   }
   red_o[sl][c4] = o;
+  red_lo[sl][c4] = ol;
   if (c4 == 0) red_l[sl] = L;
   __syncthreads();
   if (tid < DW / 4) {
-    float4 t = red_o[0][tid];
+    float4 t = red_o[0][tid], tl = red_lo[0][tid];
     float Lt = red_l[0];
 #pragma unroll
     for (int k = 1; k < SL; ++k) {
-      const float4 u = red_o[k][tid];
-      t.x += u.x;
-      t.y += u.y;
-      t.z += u.z;
-      t.w += u.w;
+      const float4 u = red_o[k][tid], ul = red_lo[k][tid];
+      two_sum_acc(t.x, tl.x, u.x);
+      two_sum_acc(t.y, tl.y, u.y);
+      two_sum_acc(t.z, tl.z, u.z);
+      two_sum_acc(t.w, tl.w, u.w);
+      tl.x += ul.x;
+      tl.y += ul.y;
+      tl.z += ul.z;
+      tl.w += ul.w;
       Lt += red_l[k];
     }
+    t.x += tl.x;
+    t.y += tl.y;
+    t.z += tl.z;
+    t.w += tl.w;
     const float vs = p.v_scale_dev ? *p.v_scale_dev : p.v_scale;
     const bool any = Lt != 0.f;  // NaN (a NaN byte in a seen token) propagates
     const float f = any ? vs / Lt : 0.f;

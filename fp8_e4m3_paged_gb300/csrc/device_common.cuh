@@ -10,6 +10,20 @@ namespace fp8kv {
 // log2(e): logits are kept in base-2 units so that softmax uses exp2.
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The base-2 logit factor softmax_scale * k_scale * log2(e) as an unevaluated
+// sum hi + lo of two FP32 values: the product is formed in double once per
+// CTA, so an exponent built from both parts keeps the precision of the exact
+// factor (a single FP32 factor carries a relative error of up to ~2^-23,
+// which shifts every weight by a few units in the last place).
+struct LogitScale {
+  float hi, lo;
+};
+__device__ __forceinline__ LogitScale logit_scale(float softmax_scale, float k_scale) {
+  const double c = (double)softmax_scale * (double)k_scale * 1.4426950408889634074;
+  const float hi = (float)c;
+  return {hi, (float)(c - (double)hi)};
+}
+
 // Exact E4M3 -> FP32 for the four bytes of w (little-endian order).
 //
 // An E4M3 byte s.eeee.mmm placed so that eeee lands in the low four bits of
@@ -63,14 +77,16 @@ __device__ __forceinline__ void set_status(unsigned int* status, unsigned int bi
 }
 
 // hi + lo += x without rounding loss in the hi/lo pair (Knuth's TwoSum: the
-// rounding error of hi + x is recovered exactly and folded into lo).
+// rounding error of hi + x is recovered exactly and folded into lo).  When
+// the sum is not finite the error term is meaningless (inf - inf) and is
+// dropped, so an infinity stays an infinity and a NaN stays a NaN in hi.
 __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
   const float s = __fadd_rn(hi, x);
   const float bp = __fsub_rn(s, hi);
   const float ap = __fsub_rn(s, bp);
   const float err = __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(x, bp));
   hi = s;
-  lo = __fadd_rn(lo, err);
+  lo = __fadd_rn(lo, fabsf(s) < INFINITY ? err : 0.f);
 }
 
 // 2^x for an integer-valued x <= 0 (running maxima are kept integral), exact.

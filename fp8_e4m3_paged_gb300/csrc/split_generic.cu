@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
 
   // ---------------------------------------------------------- Q, row lengths
   const float ks = p.k_scale_dev ? *p.k_scale_dev : p.k_scale;
-  const float c = p.softmax_scale * ks * kLog2e;
+  const LogitScale cs = logit_scale(p.softmax_scale, ks);
+  const float c = cs.hi;
   for (int idx = tid; idx < RCMAX * D; idx += NT) {
     const int i = idx / D, d = idx % D;
     float v = 0.f;
@@ -142,11 +143,18 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
 #pragma unroll
   for (int k = 0; k < RPW; ++k) { m_run[k] = -INFINITY; l_run[k] = 0.f; }
 
-  // PV accumulators: thread owns columns dg*4..+3 of rows rg + k*RG
+  // PV accumulators: thread owns columns dg*4..+3 of rows rg + k*RG.  With
+  // few rows per thread (the decode shapes this path serves) each tile is
+  // summed in FP32 on its own and added to a compensated pair acc + acc_lo
+  // (TwoSum), so the rounding of the running sum over a long partition is
+  // recovered; larger row chunks accumulate in plain FP32.
+  constexpr bool kComp = RPT <= 4;
   const int dg = tid % DG, rg = tid / DG;
-  float4 acc[RPT];
+  float4 acc[RPT], acc_lo[kComp ? RPT : 1];
 #pragma unroll
   for (int k = 0; k < RPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < (kComp ? RPT : 1); ++k) acc_lo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   __syncthreads();
 
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
         // combine's partition weights are then exact powers of two
         const float m_new = fmaxf(m_run[k], ceilf(mt));
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float arg = fmaf(lo[k], c, fmaf(hi[k], c, -m_use));
+        const float arg = fmaf(hi[k], cs.hi, -m_use) + fmaf(lo[k], cs.hi, hi[k] * cs.lo);
         const float pv = vis ? exp2f(arg) : -0.f;  // -0.0 marks "not seen"
         const float alpha = (m_run[k] == -INFINITY) ? 0.f : exp2_int(m_run[k] - m_use);
         float ps = pv;
@@ -289,12 +297,17 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
 
     // ------------------------------------------------------ PV
     {
+      float4 tt[RPT];  // this tile's sums (compensated path) or the running sums
 #pragma unroll
       for (int k = 0; k < RPT; ++k) {
         const int i = rg + k * RG;
-        if (i < RCMAX) {
-          const float a = Al[i];
-          acc[k].x *= a; acc[k].y *= a; acc[k].z *= a; acc[k].w *= a;
+        const float a = (i < RCMAX) ? Al[i] : 1.f;
+        acc[k].x *= a; acc[k].y *= a; acc[k].z *= a; acc[k].w *= a;
+        if constexpr (kComp) {
+          acc_lo[k].x *= a; acc_lo[k].y *= a; acc_lo[k].z *= a; acc_lo[k].w *= a;
+          tt[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          tt[k] = acc[k];
         }
       }
       if (!vflag) {
@@ -306,10 +319,10 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
             const int i = rg + k * RG;
             if (i < RCMAX) {
               const float pv = Ps[t * (RCMAX + 1) + i];
-              acc[k].x = fmaf(pv, v4.x, acc[k].x);
-              acc[k].y = fmaf(pv, v4.y, acc[k].y);
-              acc[k].z = fmaf(pv, v4.z, acc[k].z);
-              acc[k].w = fmaf(pv, v4.w, acc[k].w);
+              tt[k].x = fmaf(pv, v4.x, tt[k].x);
+              tt[k].y = fmaf(pv, v4.y, tt[k].y);
+              tt[k].z = fmaf(pv, v4.z, tt[k].z);
+              tt[k].w = fmaf(pv, v4.w, tt[k].w);
             }
           }
         }
@@ -323,13 +336,24 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
             if (i < RCMAX) {
               const float pv = Ps[t * (RCMAX + 1) + i];
               if (__float_as_uint(pv) != 0x80000000u) {
-                acc[k].x = fmaf(pv, v4.x, acc[k].x);
-                acc[k].y = fmaf(pv, v4.y, acc[k].y);
-                acc[k].z = fmaf(pv, v4.z, acc[k].z);
-                acc[k].w = fmaf(pv, v4.w, acc[k].w);
+                tt[k].x = fmaf(pv, v4.x, tt[k].x);
+                tt[k].y = fmaf(pv, v4.y, tt[k].y);
+                tt[k].z = fmaf(pv, v4.z, tt[k].z);
+                tt[k].w = fmaf(pv, v4.w, tt[k].w);
               }
             }
           }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) {
+        if constexpr (kComp) {
+          two_sum_acc(acc[k].x, acc_lo[k].x, tt[k].x);
+          two_sum_acc(acc[k].y, acc_lo[k].y, tt[k].y);
+          two_sum_acc(acc[k].z, acc_lo[k].z, tt[k].z);
+          two_sum_acc(acc[k].w, acc_lo[k].w, tt[k].w);
+        } else {
+          acc[k] = tt[k];
         }
       }
     }
@@ -340,7 +364,14 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
 #pragma unroll
   for (int k = 0; k < RPT; ++k) {
     const int i = rg + k * RG;
-    if (i < RC) reinterpret_cast<float4*>(acc_out + (int64_t)i * D)[dg] = acc[k];
+    float4 o = acc[k];
+    if constexpr (kComp) {
+      o.x += acc_lo[k].x;
+      o.y += acc_lo[k].y;
+      o.z += acc_lo[k].z;
+      o.w += acc_lo[k].w;
+    }
+    if (i < RC) reinterpret_cast<float4*>(acc_out + (int64_t)i * D)[dg] = o;
   }
   if (lane == 0) {
 #pragma unroll

@@ -7,47 +7,48 @@
 //                (cp.async.bulk) of a tile's E4M3 K (V) rows from the paged
 //                cache into that stream's raw shared-memory ring, completion
 //                counted in bytes on an mbarrier; runs of tokens contiguous
-//                in a page move as one copy and tokens no query row may see
-//                are never copied;
+//                in a page move as one copy, tokens no query row may see are
+//                never copied, and the page walk of the next tile is loaded
+//                while the current one waits for its stage;
 //   warps 4-7    K decoders and
-//   warps 8-11   V decoders: raw E4M3 -> exact fp16 with the hardware
-//                e4m3x2 -> f16x2 conversion into swizzled operand tiles of
-//                the stream's ring (tokens that were not copied become
-//                zeros).  K and V have separate rings and producers because
-//                different MMAs free them: a K tile is free once its QK is
-//                done, a V tile only once its PV is;
-//   warp 12      TMEM allocation and UMMA issue (one thread), in a fixed
-//                order: the QK of pair m+1, then the PVs of pair m.  The
-//                thread waits on the mbarriers itself; every chain depends
-//                only on chains issued before it, so the order cannot
-//                deadlock, and the next pair's S is ready while the softmax
-//                still works on the current pair;
+//   warps 8-11   V decoders: take a raw tile into registers and hand the raw
+//                stage straight back, then convert E4M3 -> exact fp16 with the
+//                hardware e4m3x2 -> f16x2 conversion into swizzled operand
+//                tiles of the stream's ring (tokens that were not copied
+//                become zeros).  K and V have separate rings because different
+//                MMAs free them: a K pair once its QK is done, a V tile once
+//                its PV is;
+//   warp 12      TMEM allocation and UMMA issue (one thread), issuing
+//                whichever of the next QK (per pair) and the next PV (per
+//                tile) is ready;
 //   warps 0-3    softmax: read S from TMEM, online softmax with FP32 state,
 //                write P = P_hi + P_lo (two fp16 halves) back to TMEM in place
-//                of S, rescale O (and the pair partner's P) when the running
-//                max jumps, epilogue.
+//                of S, rescale O when the running max moves, epilogue; Q is
+//                staged by warps 0-11 after the setup barrier, so the
+//                producers start without waiting for it.
 // Per pair of 64-token tiles (2m, 2m+1):
 //   QK:  S[64 x 128] = Q[64 x D] . [K(2m); K(2m+1)]^T  (one UMMA chain, M=64,
 //        N=128: A = Q resident in shared memory, B = the pair's K tiles,
 //        interleaved per column block, both K-major; N=64 for a last single
 //        tile).  Query vector 16w+j (j < 16) lands in TMEM lane 32w+j.
-//   PV:  O[128 x D] += P[128 x 64] . V[64 x D] per tile (M=128, A from TMEM,
-//        B = V tile MN-major), both tiles of the pair issued together once
-//        both P are written.  P_hi of vector 16w+j sits in lane 32w+j and its
+// Per tile i:
+//   PV:  O[128 x D] += P[128 x 64] . V[64 x D]  (M=128, A from TMEM, B = V
+//        tile MN-major).  P_hi of vector 16w+j sits in lane 32w+j and its
 //        P_lo twin in lane 32w+16+j, so one MMA accumulates both halves of
 //        the probability split; the epilogue adds the two accumulator rows.
-// Barriers are per pair: the rings hold pairs of tiles and the QK, P and PV
-// of a pair complete together.
-// TMEM: four S/P buffers of 64 columns (P(i) overwrites S(i) in buffer i%4,
-// hi in the lanes the M=64 QK writes, lo in the 16 lanes above) and O.  With
-// four buffers the QK of pair m+2 is the first to wait for the PVs of pair
-// m, so QK, softmax and PV of neighbouring pairs overlap.
+// TMEM: four S/P buffers of 64 columns (tile i uses buffer i % 4; P(i)
+// overwrites S(i), hi in the lanes the M=64 QK writes, lo in the 16 lanes
+// above) and O.  With four buffers the QK of pair m+2 is the first to wait
+// for the PVs of pair m, so QK, softmax and PV of neighbouring tiles overlap.
 // The hi/lo split keeps probabilities to ~22 bits ("compensated
 // probabilities"); the FP32 partition numerator, max and sum follow the FP32
 // state contract ("DFlash2 E4M3 attention with FP32 state", intro paragraph
 // 4).  The running max is an integer (base-2 units) that only moves when a
 // tile exceeds it by more than kTau, so P <= 2^kTau always fits fp16 and the
-// rescale factor of O is an exact power of two.
+// rescale factor of O is an exact power of two.  The softmax first forms the
+// exponents against the running max and takes a slow path (row maxima,
+// possibly a rescale of O after the previous tile's PV) only when some
+// exponent exceeds kTau, which in practice is a row's first visible tile.
 //
 // Every wait is bounded.  A wait that gives up sets a CTA-wide abort flag and
 // FP8KV_STATUS_TIMEOUT; every role then stops issuing work, the producers wait
@@ -94,7 +95,7 @@ constexpr uint32_t kWaitLimit = 1u << 20;      // polls per wait (product path)
 constexpr uint32_t kTestWaitLimit = 1u << 12;  // polls per wait under FP8KV_TEST_STALL_PIPELINE
 constexpr uint32_t kDrainLimit = 1u << 20;     // polls for issued copies / UMMAs to complete
 constexpr int kMaxStages = 4;
-constexpr int kSBuf = 4;            // S/P buffers in TMEM
+constexpr int kSBuf = 4;            // S/P buffers in TMEM (tile i uses buffer i % 4)
 
 template <int D>
 struct Cfg {
@@ -121,21 +122,21 @@ struct Cfg {
 };
 
 struct Meta {
-  // operand rings, one barrier pair per two stages (a pair of tiles)
+  // K operand ring: one barrier pair per pair slot (a QK reads both tiles)
   uint64_t k_full[kMaxStages / 2], k_empty[kMaxStages / 2];
-  uint64_t v_full[kMaxStages / 2], v_empty[kMaxStages / 2];
+  // V operand ring: one barrier pair per tile stage (PVs run per tile)
+  uint64_t v_full[kMaxStages], v_empty[kMaxStages];
   uint64_t rawk_full[kMaxStages], rawv_full[kMaxStages];
   uint64_t rawk_empty[kMaxStages], rawv_empty[kMaxStages];
-  // per pair of S/P buffers (tiles 2m, 2m+1 use buffers 2(m%2), 2(m%2)+1)
-  uint64_t s_full[2];                   // the pair's QK done
-  uint64_t p_ready[2];                  // both tiles' P written
-  uint64_t pv_done[2];                  // the pair's PVs done
+  uint64_t s_full[2];                   // per pair of S buffers: the pair's QK done
+  uint64_t p_ready[kSBuf];              // per tile buffer: its P written
+  uint64_t pv_done[kSBuf];              // per tile buffer: its PV done
   uint32_t tmem;
   uint64_t validk[kMaxStages];          // per raw K stage: tokens that were copied
   uint64_t validv[kMaxStages];          // the same for the raw V stage
-  uint32_t pmask[2][kE];                // sparse: entry masks of the tile each stream copies
   int32_t nrow[kRows];                  // dense: live length of each query vector; sparse: its query row
   uint64_t drain;                       // the MMA thread's final commit (all its UMMAs done)
+  uint64_t q_full;                      // the Q tile is in shared memory
   uint32_t abort;                       // a wait gave up: every role stops
   uint32_t vbad;                        // a V decoder met a non-finite code
 };
@@ -167,37 +168,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
   return __half22float2(*reinterpret_cast<__half2*>(&v));
-}
-
-// Scale one half of a P tile in place: 16 lanes x 32 columns of f16x2 in the
-// 16x128b layout (thread t holds, per repeat g, lane t/4 column 4g + t%4 in
-// register 2g, then lane t/4 + 8 in register 2g+1); the rows of lane t/4 are
-// multiplied by al_a, those of lane t/4 + 8 by al_b.  Both factors are powers
-// of two, so the products are exact down to the fp16 subnormal range.
-__device__ __forceinline__ void scale_p_half(uint32_t taddr, float al_a, float al_b) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x128b.x8.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float al = (j & 1) ? al_b : al_a;
-    __half2 v = *reinterpret_cast<const __half2*>(&r[j]);
-    const float2 f = __half22float2(v);
-    v = __floats2half2_rn(f.x * al, f.y * al);
-    r[j] = *reinterpret_cast<const uint32_t*>(&v);
-  }
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
 }
 
 // Both halves of P (hi rows at taddr_hi, lo rows at taddr_lo), one wait.
@@ -244,41 +214,40 @@ __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
   return r;
 }
 
-// Decode one raw tile (kT rows of D E4M3 bytes) into a swizzled fp16 operand
-// tile with the kDecThreads threads of a stream: column block db = d/64 holds
-// kT rows of 128 bytes, DBS bytes after the previous block; the 16-byte chunk c of row t sits at chunk position
-// c ^ (t % 8).  Thread lt always takes raw chunk c = lt % (D/16) of rows
-// lt / (D/16) + k * R (R = rows per pass of all threads), so every address
-// is a per-thread base plus a compile-time offset; all loads are issued
-// before the first conversion.  Rows whose bit in `valid` is clear were not
-// copied and become zeros.  With CHECK (the V stream) a non-finite code is
-// written as 0 and `bad` is set (see the kernel's header).
-template <int D, int DBS, int FMT, bool CHECK>
-__device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uint64_t valid, int lt, bool& bad) {
-  constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
-  constexpr int kR = kDecThreads / kChunks; // rows per pass
-  constexpr int kPer = kT / kR;             // chunks per thread
+// Decoding one raw tile (kT rows of D E4M3 bytes) into a swizzled fp16
+// operand tile with the kDecThreads threads of a stream: column block db =
+// d/64 holds kT rows of 128 bytes, DBS bytes after the previous block; the
+// 16-byte chunk c of row t sits at chunk position c ^ (t % 8).  Thread lt
+// always takes raw chunk c = lt % (D/16) of rows lt / (D/16) + k * R (R =
+// rows per pass of all threads), so every address is a per-thread base plus
+// a compile-time offset.  It runs in two steps: load_raw brings the thread's
+// raw chunks into registers (after which the raw stage may be refilled), and
+// store_tile converts and stores them.  Rows whose bit in `valid` is clear
+// were not copied and become zeros.  With CHECK (the V stream) a non-finite
+// code is written as 0 and `bad` is set (see the kernel's header).
+template <int D>
+struct DecShape {
+  static constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
+  static constexpr int kR = kDecThreads / kChunks; // rows per pass
+  static constexpr int kPer = kT / kR;             // chunks per thread
   static_assert(kDecThreads % kChunks == 0 && kT % kR == 0, "decoder shape");
-  const int c = lt % kChunks, t0 = lt / kChunks;
-  const int db = c / 4;
-  const int h0 = (c % 4) * 2;  // first of the two 16-byte fp16 chunks
-  // alternate the order of the two stores between column blocks so the
-  // eight threads of a store phase hit eight different bank groups
-  const bool swap = (db & 1) != 0;
-  const int first = swap ? h0 + 1 : h0;
-  const int second = swap ? h0 : h0 + 1;
+};
+
+template <int D, int FMT, bool CHECK>
+__device__ __forceinline__ void load_raw(const uint8_t* raw, uint64_t valid, int lt, uint4 (&w)[DecShape<D>::kPer],
+                                         bool& bad) {
+  using S = DecShape<D>;
+  const int c = lt % S::kChunks, t0 = lt / S::kChunks;
   const uint8_t* src = raw + t0 * D + c * 16;
-  uint8_t* dst = op + db * DBS + t0 * 128;
   const bool full = valid == ~0ull;
-  uint4 w[kPer];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    w[k] = (full || ((valid >> (t0 + k * kR)) & 1ull)) ? *reinterpret_cast<const uint4*>(src + k * kR * D)
-                                                      : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < S::kPer; ++k) {
+    w[k] = (full || ((valid >> (t0 + k * S::kR)) & 1ull)) ? *reinterpret_cast<const uint4*>(src + k * S::kR * D)
+                                                         : make_uint4(0, 0, 0, 0);
   }
   if (CHECK) {
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
+    for (int k = 0; k < S::kPer; ++k) {
       if (nonfinite_codes(w[k], FMT == FP8KV_KV_E5M2) != 0u) {
         bad = true;
         w[k].x = zap_nonfinite(w[k].x, FMT == FP8KV_KV_E5M2);
@@ -288,24 +257,59 @@ __device__ __forceinline__ void decode_tile(const uint8_t* raw, uint8_t* op, uin
       }
     }
   }
+}
+
+template <int D, int DBS, int FMT>
+__device__ __forceinline__ void store_tile(uint8_t* op, const uint4 (&w)[DecShape<D>::kPer], int lt) {
+  using S = DecShape<D>;
+  const int c = lt % S::kChunks, t0 = lt / S::kChunks;
+  const int db = c / 4;
+  const int h0 = (c % 4) * 2;  // first of the two 16-byte fp16 chunks
+  // alternate the order of the two stores between column blocks so the
+  // eight threads of a store phase hit eight different bank groups
+  const bool swap = (db & 1) != 0;
+  const int first = swap ? h0 + 1 : h0;
+  const int second = swap ? h0 : h0 + 1;
+  uint8_t* dst = op + db * DBS + t0 * 128;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int sw = (t0 + k * kR) & 7;
-    uint8_t* row = dst + k * kR * 128;
+  for (int k = 0; k < S::kPer; ++k) {
+    const int sw = (t0 + k * S::kR) & 7;
+    uint8_t* row = dst + k * S::kR * 128;
     const uint4 x0 = dec8<FMT>(w[k].x, w[k].y), x1 = dec8<FMT>(w[k].z, w[k].w);
     *reinterpret_cast<uint4*>(row + ((first ^ sw) * 16)) = swap ? x1 : x0;
     *reinterpret_cast<uint4*>(row + ((second ^ sw) * 16)) = swap ? x0 : x1;
   }
 }
 
+// Block ids of the first two pages a dense tile touches, loaded one tile
+// ahead of its copies so that the page walk does not wait for a global load
+// between a raw stage becoming free and its refill (a tile with larger
+// pages touches at most two; smaller pages load the rest on the spot).
+struct TilePages {
+  int page0;
+  int blk[2];
+};
+
+__device__ __forceinline__ TilePages fetch_pages(const Params& p, int b, int u0, int u1, int i) {
+  TilePages tp;
+  const int tok0 = u0 + i * kT;
+  tp.page0 = tok0 / p.page_size;
+  const int last = (min(u1, tok0 + kT) - 1) / p.page_size;
+  const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride;
+  tp.blk[0] = tok0 < u1 ? bt[tp.page0] : -1;
+  tp.blk[1] = (tok0 < u1 && last > tp.page0) ? bt[tp.page0 + 1] : -1;
+  return tp;
+}
+
 // Issue the bulk copies of one tile's K (or V) rows into a raw stage and
 // return the set of token slots that were copied.  Dense: runs of tokens
 // contiguous in a page; sparse: the tokens of each entry that some query row
-// attends (the tile's masks, already checked, are in `masks`).
+// attends (the tile's checked masks and microblock ids are in mk / bk).
 template <int D, int MODE>
 __device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* cache, int64_t sb, int64_t st,
                                               int64_t sh, int b, int g, int u0, int u1, int i, uint8_t* dst,
-                                              uint64_t* bar, const uint32_t* masks, bool report) {
+                                              uint64_t* bar, const TilePages& tp, const uint32_t (&mk)[kE],
+                                              const int (&bk)[kE], bool report) {
   uint64_t valid = 0ull;
   if (MODE == FP8KV_MODE_DENSE) {
     int t = 0;
@@ -313,7 +317,8 @@ __device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* ca
       const int tok = u0 + i * kT + t;
       if (tok >= u1) break;
       const int page = tok / p.page_size, slot_in = tok % p.page_size;
-      const int blk = p.block_table[(int64_t)b * p.bt_stride + page];
+      const int dp = page - tp.page0;
+      const int blk = dp == 0 ? tp.blk[0] : dp == 1 ? tp.blk[1] : p.block_table[(int64_t)b * p.bt_stride + page];
       const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
       if (blk >= 0 && blk < p.num_kv_blocks) {
         const uint8_t* src = cache + blk * sb + slot_in * st + g * sh;
@@ -334,15 +339,14 @@ __device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* ca
       t += run;
     }
   } else {
+#pragma unroll
     for (int el = 0; el < kE; ++el) {
-      const uint32_t mk = masks[el];
-      if (mk == 0u) continue;
-      const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + u0 + i * kE + el];
+      if (mk[el] == 0u) continue;
       for (int tk = 0; tk < 4; ++tk) {
-        if ((mk & (0x11111111u << tk)) == 0u) continue;
+        if ((mk[el] & (0x11111111u << tk)) == 0u) continue;
         const int t = el * 4 + tk;
         mbar_expect_tx(bar, D);
-        bulk_g2s(dst + t * D, cache + blk * sb + tk * st + g * sh, D, bar);
+        bulk_g2s(dst + t * D, cache + bk[el] * sb + tk * st + g * sh, D, bar);
         valid |= 1ull << t;
       }
     }
@@ -356,8 +360,8 @@ __device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* ca
 // tokens below the longest row, sparse the tokens some row sees), and for
 // each non-finite byte (token t, column d) marks every query vector i that
 // sees t; then element (i, d) of the numerator becomes NaN (a NaN code, or
-// infinities of both signs) or +-infinity.  `scratch` holds one byte per
-// (vector, column): bit 0 NaN, bit 1 +inf, bit 2 -inf.
+// infinities of both signs) or +-infinity.  `scratch` holds one byte per (vector, column):
+// bit 0 NaN, bit 1 +inf, bit 2 -inf.
 template <int D, int MODE, int FMT>
 __device__ __noinline__ void patch_nonfinite_v(const Params& p, uint8_t* scratch, const int32_t* nrow, int b, int g,
                                                int u0, int u1, int RC, int64_t prow) {
@@ -434,22 +438,38 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 
   // ---------------------------------------------------------- loads
   // Everything the setup reads from global memory is requested up front,
-  // so its latencies overlap: this thread's share of the Q tile, the live
-  // length (or query row) of query vector tid, and the row lengths that
-  // fix the partition range.
+  // so its latencies overlap: the Q tile (warps below the MMA warp, which
+  // store it only after the barrier below: the producers need not wait for
+  // it), the live length (or query row) of query vector tid, and the row
+  // lengths that fix the partition range.
+  constexpr int kQThreads = 32 * kMmaWarp;                      // warps 0..11
   constexpr int kQChunks = kRows * (D / 8);                     // 16-byte Q chunks
-  constexpr int kQPer = (kQChunks + kThreads - 1) / kThreads;
+  constexpr int kQPer = (kQChunks + kQThreads - 1) / kQThreads;
   uint4 qv[kQPer];
+  if (tid < kQThreads) {
 #pragma unroll
-  for (int k = 0; k < kQPer; ++k) {
-    const int idx = tid + k * kThreads;
-    const int i = idx / (D / 8), c8 = idx % (D / 8);  // row, 8-element chunk
-    qv[k] = make_uint4(0, 0, 0, 0);
-    if (idx < kQChunks && i < RC) {
-      const int rowi = row0 + i;
-      const int r = rowi / p.G, h = g * p.G + rowi % p.G;
-      qv[k] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D + c8 * 8);
+    for (int k = 0; k < kQPer; ++k) {
+      const int idx = tid + k * kQThreads;
+      const int i = idx / (D / 8), c8 = idx % (D / 8);  // row, 8-element chunk
+      qv[k] = make_uint4(0, 0, 0, 0);
+      if (idx < kQChunks && i < RC) {
+        const int rowi = row0 + i;
+        const int r = rowi / p.G, h = g * p.G + rowi % p.G;
+        qv[k] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.q_max + r) * p.Hq + h) * D + c8 * 8);
+      }
     }
+  }
+  // Dense producers: the block ids of the first tile, assuming that the
+  // longest row has the planned maximum length (the usual case); checked
+  // against the real range below and loaded again when it differs.
+  TilePages tp_spec = {-1, {-1, -1}};
+  int u0_spec = 0, u1_spec = 0;
+  if (MODE == FP8KV_MODE_DENSE && (warp == kProdWarp || warp == kProdWarp + 1) && lane == 0) {
+    int per_s = (p.max_kv_len + p.S - 1) / p.S;
+    per_s = (per_s + kT - 1) / kT * kT;
+    u0_spec = s * per_s;
+    u1_spec = min(p.max_kv_len, u0_spec + per_s);
+    if (u0_spec < u1_spec) tp_spec = fetch_pages(p, b, u0_spec, u1_spec, 0);
   }
   int my_nrow = -1;
   if (tid < RC) {
@@ -494,11 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   // ---------------------------------------------------------- setup
   if (tid == 0) {
     for (int i = 0; i < C::kKStages / 2; ++i) {
-      mbar_init(&mt.k_full[i], 2 * kDecThreads);
+      mbar_init(&mt.k_full[i], 2 * kDecThreads);  // every decoder thread, both tiles of the pair
       mbar_init(&mt.k_empty[i], 1);
     }
-    for (int i = 0; i < C::kVStages / 2; ++i) {
-      mbar_init(&mt.v_full[i], 2 * kDecThreads);
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&mt.v_full[i], kDecThreads);
       mbar_init(&mt.v_empty[i], 1);
     }
     for (int i = 0; i < C::kRaw; ++i) {
@@ -507,11 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       mbar_init(&mt.rawk_empty[i], kDecThreads);
       mbar_init(&mt.rawv_empty[i], kDecThreads);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&mt.s_full[i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&mt.s_full[i], 1);
+    for (int i = 0; i < kSBuf; ++i) {
       mbar_init(&mt.pv_done[i], 1);
-      mbar_init(&mt.p_ready[i], 2 * 32 * kSoftmaxWarps);
+      mbar_init(&mt.p_ready[i], 32 * kSoftmaxWarps);
     }
+    mbar_init(&mt.q_full, kQThreads);
     mbar_init(&mt.drain, 1);
     mt.abort = 0u;
     mt.vbad = 0u;
@@ -523,24 +544,29 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   }
   static_assert(kRows <= kThreads, "one query vector per thread");
   if (tid < kRows) mt.nrow[tid] = my_nrow;
-  // Q rows -> swizzled K-major tile in shared memory (rows >= RC are zero)
-  uint8_t* sQ = smem + C::kOffQ;
-#pragma unroll
-  for (int k = 0; k < kQPer; ++k) {
-    const int idx = tid + k * kThreads;
-    if (idx < kQChunks) {
-      const int i = idx / (D / 8), c8 = idx % (D / 8);
-      const int db = c8 / 8, ch = c8 % 8;
-      *reinterpret_cast<uint4*>(sQ + db * (kRows * 128) + i * 128 + ((ch ^ (i & 7)) * 16)) = qv[k];
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = mt.tmem;
   volatile uint32_t* const abort_flag = &mt.abort;
   const uint32_t wlim = (p.test_flags & FP8KV_TEST_STALL_PIPELINE) ? kTestWaitLimit : kWaitLimit;
+
+  if (tid < kQThreads) {
+    // Q rows -> swizzled K-major tile in shared memory (rows >= RC are zero);
+    // the MMA thread waits for q_full before the first QK
+    uint8_t* sQ = smem + C::kOffQ;
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int idx = tid + k * kQThreads;
+      if (idx < kQChunks) {
+        const int i = idx / (D / 8), c8 = idx % (D / 8);
+        const int db = c8 / 8, ch = c8 % 8;
+        *reinterpret_cast<uint4*>(sQ + db * (kRows * 128) + i * 128 + ((ch ^ (i & 7)) * 16)) = qv[k];
+      }
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&mt.q_full);
+  }
 
   if (warp == kProdWarp || warp == kProdWarp + 1) {
     // ======================================================== producers
@@ -552,22 +578,37 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
       const int64_t csb = is_k ? p.ksb : p.vsb, cst = is_k ? p.kst : p.vst, csh = is_k ? p.ksh : p.vsh;
       uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
-      uint32_t* masks = mt.pmask[is_k ? 0 : 1];
       bool ok = true;
       int issued = 0;  // tiles whose copies were issued
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const int slot = i % C::kRaw;
-        if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
-          // entry masks of the tile (all loads first); an entry with a bad
-          // block contributes nothing
-          uint32_t mk[kE];
-          int bk[kE];
+      // the page walk of tile i + 1 (block ids, or sparse entries) is loaded
+      // while tile i waits for its stage
+      TilePages tp = {0, {-1, -1}};
+      uint32_t mk[kE];
+      int bk[kE];
+      auto fetch = [&](int i, TilePages& t, uint32_t (&m)[kE], int (&k)[kE]) {
+        if (MODE == FP8KV_MODE_DENSE) {
+          t = fetch_pages(p, b, u0, u1, i);
+        } else {
 #pragma unroll
           for (int el = 0; el < kE; ++el) {
             const int e = u0 + i * kE + el;
-            mk[el] = (e < u1) ? p.entry_mask[(int64_t)b * p.entry_stride + e] : 0u;
-            bk[el] = (e < u1) ? p.entry_tbl[(int64_t)b * p.entry_stride + e] : 0;
+            m[el] = (e < u1) ? p.entry_mask[(int64_t)b * p.entry_stride + e] : 0u;
+            k[el] = (e < u1) ? p.entry_tbl[(int64_t)b * p.entry_stride + e] : 0;
           }
+        }
+      };
+      if (MODE == FP8KV_MODE_DENSE && u0 == u0_spec && u1 == u1_spec)
+        tp = tp_spec;
+      else
+        fetch(0, tp, mk, bk);
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int slot = i % C::kRaw;
+        TilePages tp_next = {0, {-1, -1}};
+        uint32_t mk_next[kE];
+        int bk_next[kE];
+        if (i + 1 < n_tiles) fetch(i + 1, tp_next, mk_next, bk_next);
+        if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
+          // an entry with a bad block contributes nothing
 #pragma unroll
           for (int el = 0; el < kE; ++el) {
             if (mk[el] != 0u && (bk[el] < 0 || bk[el] >= p.num_kv_blocks)) {
@@ -575,22 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
               mk[el] = 0u;
             }
           }
-          // the masks are read only by this thread, after the stage is free
-          if (i >= C::kRaw && !mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int el = 0; el < kE; ++el) masks[el] = mk[el];
-        } else if (i >= C::kRaw) {
-          // the raw stage is free once the decoders took its previous tile
-          if (!mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag)) {
-            ok = false;
-            break;
-          }
+        }
+        // the raw stage is free once the decoders loaded its previous tile
+        if (i >= C::kRaw && !mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag)) {
+          ok = false;
+          break;
         }
         valid[slot] = copy_rows<D, MODE>(p, cache, csb, cst, csh, b, g, u0, u1, i,
-                                         raw_base + slot * C::kRawBytes, &raw_full[slot], masks, is_k);
+                                         raw_base + slot * C::kRawBytes, &raw_full[slot], tp, mk, bk, is_k);
         issued = i + 1;
         if (is_k && i == 0 && (p.test_flags & FP8KV_TEST_STALL_PIPELINE)) {
           // test only: hold back this arrival until a waiting warp has given
@@ -600,6 +633,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
           break;
         }
         mbar_arrive(&raw_full[slot]);
+        tp = tp_next;
+#pragma unroll
+        for (int el = 0; el < kE; ++el) {
+          mk[el] = mk_next[el];
+          bk[el] = bk_next[el];
+        }
       }
       // Drain: the copies of the last tile of every stage must have landed
       // before the CTA may exit (the decoders normally consumed them already;
@@ -617,8 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     const int n_stages = is_k ? C::kKStages : C::kVStages;
     uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
     uint64_t* raw_empty = is_k ? mt.rawk_empty : mt.rawv_empty;
-    uint64_t* op_full = is_k ? mt.k_full : mt.v_full;
-    uint64_t* op_empty = is_k ? mt.k_empty : mt.v_empty;
     const uint64_t* valid = is_k ? mt.validk : mt.validv;
     const uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
     uint8_t* op_base = smem + (is_k ? C::kOffK : C::kOffV);
@@ -626,96 +663,128 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
     for (int i = 0; i < n_tiles; ++i) {
       const int slot = i % C::kRaw;
       const int st = i % n_stages;
-      // raw rows arrived, and the operand stage is free (the MMA that read
-      // its previous tile, and that tile's partner, is done)
-      if (!mbar_wait(&raw_full[slot], (i / C::kRaw) & 1, wlim, abort_flag) ||
-          (i >= n_stages && !mbar_wait(&op_empty[st / 2], ((i / n_stages) - 1) & 1, wlim, abort_flag))) {
+      // raw rows arrived: take them into registers and hand the raw stage
+      // back to the producer at once, so its refill overlaps the wait for
+      // the operand stage and the conversion
+      if (!mbar_wait(&raw_full[slot], (i / C::kRaw) & 1, wlim, abort_flag)) {
         ok = false;
         break;
       }
-      if (is_k) {
-        // K stages hold pairs of tiles interleaved per column block, so that
-        // two consecutive tiles form one 128-row operand of the pair's QK
-        uint8_t* op = op_base + (st / 2) * (2 * C::kOpBytes) + (st % 2) * (kT * 128);
-        decode_tile<D, 2 * kT * 128, FMT, false>(raw_base + slot * C::kRawBytes, op, valid[slot], lt, bad);
-      } else {
-        decode_tile<D, kT * 128, FMT, true>(raw_base + slot * C::kRawBytes, op_base + st * C::kOpBytes,
-                                            valid[slot], lt, bad);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&op_full[st / 2]);
-      if ((i & 1) == 0 && i + 1 == n_tiles) mbar_arrive(&op_full[st / 2]);  // a last tile without partner
+      uint4 w[DecShape<D>::kPer];
+      if (is_k)
+        load_raw<D, FMT, false>(raw_base + slot * C::kRawBytes, valid[slot], lt, w, bad);
+      else
+        load_raw<D, FMT, true>(raw_base + slot * C::kRawBytes, valid[slot], lt, w, bad);
       mbar_arrive(&raw_empty[slot]);
+      if (is_k) {
+        // K stages hold pairs of tiles interleaved per 64-column block, so
+        // that two consecutive tiles form one 128-row operand of the pair's
+        // QK; the slot is free once the previous QK that read it is done.
+        // (Waiting per 64-column block instead was measured slower: every
+        // decoder warp holds chunks of all blocks, so its lanes diverge.)
+        const int m = i >> 1, slot = m % (C::kKStages / 2);
+        if (m >= C::kKStages / 2 &&
+            !mbar_wait(&mt.k_empty[slot], ((m / (C::kKStages / 2)) - 1) & 1, wlim, abort_flag)) {
+          ok = false;
+          break;
+        }
+        store_tile<D, 2 * kT * 128, FMT>(op_base + slot * (2 * C::kOpBytes) + (i & 1) * (kT * 128), w, lt);
+        fence_proxy_async_smem();
+        mbar_arrive(&mt.k_full[slot]);
+        if ((i & 1) == 0 && i + 1 == n_tiles) mbar_arrive(&mt.k_full[slot]);  // a last tile without partner
+      } else {
+        // the V stage is free once the PV of its previous tile is done
+        if (i >= n_stages && !mbar_wait(&mt.v_empty[st], ((i / n_stages) - 1) & 1, wlim, abort_flag)) {
+          ok = false;
+          break;
+        }
+        store_tile<D, kT * 128, FMT>(op_base + st * C::kOpBytes, w, lt);
+        fence_proxy_async_smem();
+        mbar_arrive(&mt.v_full[st]);
+      }
     }
     if (bad) mt.vbad = 1u;
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
-    // One thread issues every chain in a fixed order: QK(0), then for each
-    // pair m the QK of pair m+1 followed by the PVs of pair m.  Each chain
-    // waits only for work issued before it (K decoded, the PVs of the pair
-    // whose S/P buffers it reuses; P written, V decoded), so the order cannot
-    // deadlock, and the QK of the next pair is in flight while the softmax
-    // still works on the current one.
+    // One thread issues every UMMA.  QK of pair m: once both K tiles are
+    // decoded, the D/16 K16 steps of one chain, then commits that free the K
+    // slot and mark S full.  PV of tile i: once its P is written and its V
+    // tile decoded, four K16 steps into O, then commits that free the V stage
+    // and mark the tile's PV done.  The thread issues whichever of the next
+    // QK and the next PV is ready (the QK first when both are): every
+    // operation depends only on operations issued before it, so no order can
+    // deadlock.  Descriptors are built once; a step only adds its offset to
+    // the start-address field (shared-memory offsets stay below 2^18).
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16_f32(64, kT, false, false);
+      const uint32_t idesc_qk1 = idesc_f16_f32(64, kT, false, false);
       const uint32_t idesc_qk2 = idesc_f16_f32(64, 2 * kT, false, false);
-      const uint32_t sq = smem_u32(smem + C::kOffQ);
       const uint32_t idesc_pv = idesc_f16_f32(128, D, false, true);
+      const uint64_t qdesc = smem_desc(smem_u32(smem + C::kOffQ), 16, 1024, kSw128);
+      const uint64_t kdesc = smem_desc(smem_u32(smem + C::kOffK), 16, 1024, kSw128);
+      const uint64_t vdesc = smem_desc(smem_u32(smem + C::kOffV), kT * 128, 1024, kSw128);
+      constexpr int kPairSlots = C::kKStages / 2;
       const int n_pairs = (n_tiles + 1) / 2;
-      bool ok = true;
-      // QK of the tile pair (2m, 2m+1): S = Q . [K(2m); K(2m+1)]^T, one
-      // N=128 chain (N=64 for a last single tile)
+      bool ok = mbar_wait(&mt.q_full, 0, wlim, abort_flag);
+      tc_fence_after();
+      // S = Q . [K(2m); K(2m+1)]^T: one N=128 chain (N=64 for a last single tile)
       auto issue_qk = [&](int m) {
-        const int i0 = 2 * m;
-        const bool two = i0 + 1 < n_tiles;
-        const int st0 = i0 % C::kKStages;
-        if (!mbar_wait(&mt.k_full[st0 / 2], (i0 / C::kKStages) & 1, wlim, abort_flag) ||
-            (m >= 2 && !mbar_wait(&mt.pv_done[m & 1], ((m >> 1) - 1) & 1, wlim, abort_flag))) {
+        const int slot = m % kPairSlots;
+        const uint32_t par = (m / kPairSlots) & 1;
+        const uint32_t idesc = (2 * m + 1 < n_tiles) ? idesc_qk2 : idesc_qk1;
+        const uint32_t dcol = tmem + C::kColS + ((2 * m) % kSBuf) * kT;
+        const uint64_t kb = kdesc + (uint64_t)((slot * 2 * C::kOpBytes) >> 4);
+        if (!mbar_wait(&mt.k_full[slot], par, wlim, abort_flag)) {
           ok = false;
           return;
         }
         tc_fence_after();
-        const uint32_t sk = smem_u32(smem + C::kOffK + (st0 / 2) * (2 * C::kOpBytes));
-        const uint32_t idesc = two ? idesc_qk2 : idesc_qk;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bd = smem_desc(sk + (kk / 4) * (2 * kT * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-          const uint64_t ad = smem_desc(sq + (kk / 4) * (kRows * 128) + (kk % 4) * 32, 16, 1024, kSw128);
-          mma_ss(tmem + C::kColS + (i0 % kSBuf) * kT, ad, bd, idesc, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(dcol, qdesc + (uint64_t)(((kk / 4) * (kRows * 128) + (kk % 4) * 32) >> 4),
+                 kb + (uint64_t)(((kk / 4) * (2 * kT * 128) + (kk % 4) * 32) >> 4), idesc, kk > 0);
+        mma_commit(&mt.k_empty[slot]);
         mma_commit(&mt.s_full[m & 1]);
-        mma_commit(&mt.k_empty[st0 / 2]);
       };
-      // PVs of the pair: O += P(2m) . V(2m) [+ P(2m+1) . V(2m+1)]
-      auto issue_pv = [&](int m) {
-        const int j0 = 2 * m;
-        const int sv0 = j0 % C::kVStages;
-        if (!mbar_wait(&mt.p_ready[m & 1], (m >> 1) & 1, wlim, abort_flag) ||
-            !mbar_wait(&mt.v_full[sv0 / 2], (j0 / C::kVStages) & 1, wlim, abort_flag)) {
-          ok = false;
-          return;
-        }
+      // O += P(i) . V(i): A = P from TMEM (hi rows and their lo twins), B = V
+      auto issue_pv = [&](int i) {
+        const int st = i % C::kVStages;
         tc_fence_after();
-        for (int j = j0; j < j0 + 2 && j < n_tiles; ++j) {
-          const uint32_t sv = smem_u32(smem + C::kOffV + (j % C::kVStages) * C::kOpBytes);
+        const uint64_t vb = vdesc + (uint64_t)((st * C::kOpBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk) {
-            const uint64_t bd = smem_desc(sv + kk * (16 * 128), kT * 128, 1024, kSw128);
-            mma_ts(tmem + C::kColO, tmem + C::kColS + (j % kSBuf) * kT + kk * 8, bd, idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        mma_commit(&mt.pv_done[m & 1]);
-        mma_commit(&mt.v_empty[sv0 / 2]);
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + C::kColO, tmem + C::kColS + (i % kSBuf) * kT + kk * 8,
+                 vb + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&mt.v_empty[st]);
+        mma_commit(&mt.pv_done[i % kSBuf]);
       };
-      issue_qk(0);
-      for (int m = 0; m < n_pairs && ok; ++m) {
-        if (m + 1 < n_pairs) issue_qk(m + 1);
-        if (ok) issue_pv(m);
+      int qn = 0, pn = 0;  // next QK pair, next PV tile
+      uint32_t idle = 0;
+      while (ok && pn < n_tiles) {
+        // QK(qn) may start once block 0 of its pair is decoded and its S
+        // buffers are free (the PVs of tiles 2qn-4 and 2qn-3 are done)
+        if (qn < n_pairs && mbar_test(&mt.k_full[qn % kPairSlots], (qn / kPairSlots) & 1) &&
+            (qn < 2 || mbar_test(&mt.pv_done[(2 * qn - 3) % kSBuf], ((2 * qn - 3) / kSBuf) & 1))) {
+          issue_qk(qn++);
+          idle = 0;
+          continue;
+        }
+        // PV(pn) once its P is written and its V decoded
+        if (pn < 2 * qn && mbar_test(&mt.p_ready[pn % kSBuf], (pn / kSBuf) & 1) &&
+            mbar_test(&mt.v_full[pn % C::kVStages], (pn / C::kVStages) & 1)) {
+          issue_pv(pn++);
+          idle = 0;
+          continue;
+        }
+        if (*abort_flag || ++idle > wlim) {
+          *abort_flag = 1u;
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
       }
       // Drain: every UMMA this thread issued must be done before TMEM is
-      // freed (normally the softmax warps already waited for the last PVs).
+      // freed (normally the softmax warps already waited for the last PV).
       mma_commit(&mt.drain);
       mbar_wait_plain(&mt.drain, 0, kDrainLimit);
       if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
@@ -742,7 +811,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       if (warp_live) {
         uint32_t sr[32];
         ld_16x256b_x8(tmem + C::kColS + (i % kSBuf) * kT + lane_off, sr);
-        tmem_ld_wait();
         // visibility of this thread's 16 columns for rows ra (bits 0..15) and rb (16..31)
         uint32_t vis;
         if (MODE == FP8KV_MODE_DENSE) {
@@ -782,58 +850,87 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
             }
           }
         }
-        // a tile every column of which both rows see takes the path
-        // without per-element selects (warp-uniform)
+        // a tile every column of which both rows see skips the selects
         const bool full = __all_sync(0xffffffffu, vis == 0xFFFFFFFFu);
-        float mx_a = -INFINITY, mx_b = -INFINITY;
-        if (full) {
+        // Exponents against the running maximum (a row that has seen nothing
+        // yet uses a huge negative stand-in, so any visible element forces
+        // the slow path below); masked elements get -inf by selection, so
+        // their p is exactly 0 and a NaN logit of an unseen token is dropped.
+        float ea[16], eb[16];
+        auto exps = [&](float mua, float mub) {
 #pragma unroll
-          for (int gq = 0; gq < 8; ++gq)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * gq + e]) * c);
-              mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * gq + 2 + e]) * c);
-            }
-        } else {
-#pragma unroll
-          for (int gq = 0; gq < 8; ++gq)
+          for (int q2 = 0; q2 < 8; ++q2)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              if ((vis >> (2 * gq + e)) & 1u) mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * gq + e]) * c);
-              if ((vis >> (16 + 2 * gq + e)) & 1u) mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * gq + 2 + e]) * c);
+              const float xa = fmaf(__uint_as_float(sr[4 * q2 + e]), c, -mua);
+              const float xb = fmaf(__uint_as_float(sr[4 * q2 + 2 + e]), c, -mub);
+              ea[2 * q2 + e] = (full || ((vis >> (2 * q2 + e)) & 1u)) ? xa : -INFINITY;
+              eb[2 * q2 + e] = (full || ((vis >> (16 + 2 * q2 + e)) & 1u)) ? xb : -INFINITY;
             }
+        };
+        exps(m_a == -INFINITY ? -3.0e38f : m_a, m_b == -INFINITY ? -3.0e38f : m_b);
+        float xa = ea[0], xb = eb[0];
+#pragma unroll
+        for (int j = 1; j < 16; ++j) {
+          xa = fmaxf(xa, ea[j]);
+          xb = fmaxf(xb, eb[j]);
         }
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-        // lazy integer max
-        const float mn_a = (mx_a > m_a + kTau || m_a == -INFINITY) ? fmaxf(m_a, ceilf(mx_a)) : m_a;
-        const float mn_b = (mx_b > m_b + kTau || m_b == -INFINITY) ? fmaxf(m_b, ceilf(mx_b)) : m_b;
-        const bool resc_a = (i > 0) && (m_a != -INFINITY) && (mn_a != m_a);
-        const bool resc_b = (i > 0) && (m_b != -INFINITY) && (mn_b != m_b);
-        const float alpha_a = resc_a ? exp2_int(m_a - mn_a) : 1.f;
-        const float alpha_b = resc_b ? exp2_int(m_b - mn_b) : 1.f;
-        m_a = mn_a;
-        m_b = mn_b;
-        const float mu_a = (m_a == -INFINITY) ? 0.f : m_a;
-        const float mu_b = (m_b == -INFINITY) ? 0.f : m_b;
+        float alpha_a = 1.f, alpha_b = 1.f;
+        if (__any_sync(0xffffffffu, xa > kTau || xb > kTau)) {
+          // Slow path: some row's lazy integer maximum must move (always on
+          // a row's first visible tile).  Row maxima over the visible logits.
+          float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+          for (int q2 = 0; q2 < 8; ++q2)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              if (full || ((vis >> (2 * q2 + e)) & 1u)) mx_a = fmaxf(mx_a, __uint_as_float(sr[4 * q2 + e]) * c);
+              if (full || ((vis >> (16 + 2 * q2 + e)) & 1u))
+                mx_b = fmaxf(mx_b, __uint_as_float(sr[4 * q2 + 2 + e]) * c);
+            }
+          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+          const float mn_a = (mx_a > m_a + kTau || m_a == -INFINITY) ? fmaxf(m_a, ceilf(mx_a)) : m_a;
+          const float mn_b = (mx_b > m_b + kTau || m_b == -INFINITY) ? fmaxf(m_b, ceilf(mx_b)) : m_b;
+          const bool resc_a = (m_a != -INFINITY) && (mn_a != m_a);
+          const bool resc_b = (m_b != -INFINITY) && (mn_b != m_b);
+          alpha_a = resc_a ? exp2_int(m_a - mn_a) : 1.f;
+          alpha_b = resc_b ? exp2_int(m_b - mn_b) : 1.f;
+          m_a = mn_a;
+          m_b = mn_b;
+          exps(m_a == -INFINITY ? -3.0e38f : m_a, m_b == -INFINITY ? -3.0e38f : m_b);
+          if (__any_sync(0xffffffffu, resc_a || resc_b) && i > 0 &&
+              mbar_wait(&mt.pv_done[(i - 1) % kSBuf], ((i - 1) / kSBuf) & 1, wlim, abort_flag)) {
+            // O holds exactly the PVs of the tiles before this one (all made
+            // under the old maxima): scale it by the exact power of two.
+            // Thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16
+            // (the P_hi row for lane < 16, its P_lo twin above); the alpha of
+            // vector 16w + x lives in thread 4*(x%8), as its a (x < 8) or b value.
+            tc_fence_after();
+            const int x = lane & 15;
+            const float al_a = __shfl_sync(0xffffffffu, alpha_a, 4 * (x & 7));
+            const float al_b = __shfl_sync(0xffffffffu, alpha_b, 4 * (x & 7));
+            const float al = (x < 8) ? al_a : al_b;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t o[16];
+              tmem_ld16(tmem + C::kColO + lane_off + c0, o);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
+              tmem_st16(tmem + C::kColO + lane_off + c0, o);
+            }
+          }
+        }
+        // P = P_hi + P_lo (two fp16 halves) replaces S in the tile's buffer:
+        // hi in lanes 32w+0..15, lo 16 above
         uint32_t ph[16], pl[16];
         float sum_a = 0.f, sum_b = 0.f;
-        // masked tokens get exactly 0 by selection (never 0 * x arithmetic)
-        const uint32_t vsel = full ? 0xFFFFFFFFu : vis;
 #pragma unroll
         for (int q2 = 0; q2 < 8; ++q2) {
-          float pa0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2]), c, -mu_a));
-          float pa1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 1]), c, -mu_a));
-          float pb0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 2]), c, -mu_b));
-          float pb1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q2 + 3]), c, -mu_b));
-          if (!full) {
-            pa0 = ((vsel >> (2 * q2)) & 1u) ? pa0 : 0.f;
-            pa1 = ((vsel >> (2 * q2 + 1)) & 1u) ? pa1 : 0.f;
-            pb0 = ((vsel >> (16 + 2 * q2)) & 1u) ? pb0 : 0.f;
-            pb1 = ((vsel >> (17 + 2 * q2)) & 1u) ? pb1 : 0.f;
-          }
+          const float pa0 = fast_exp2(ea[2 * q2]), pa1 = fast_exp2(ea[2 * q2 + 1]);
+          const float pb0 = fast_exp2(eb[2 * q2]), pb1 = fast_exp2(eb[2 * q2 + 1]);
           sum_a += pa0 + pa1;
           sum_b += pb0 + pb1;
           const uint32_t ha = pack_f16x2(pa0, pa1), hb = pack_f16x2(pb0, pb1);
@@ -849,58 +946,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         sum_b += __shfl_xor_sync(0xffffffffu, sum_b, 2);
         l_a = l_a * alpha_a + sum_a;
         l_b = l_b * alpha_b + sum_b;
-
-        if (__any_sync(0xffffffffu, resc_a || resc_b)) {
-          // PVs run per pair of tiles: O holds the pairs before this tile's
-          // pair once their PVs are done, and for an odd tile the partner's P,
-          // made under the previous max, has not gone through its PV yet.
-          const int m = i >> 1;
-          if (m >= 1 && mbar_wait(&mt.pv_done[(m - 1) & 1], ((m - 1) >> 1) & 1, wlim, abort_flag)) {
-            tc_fence_after();
-            // thread `lane` owns TMEM lane 32w + lane = vector 16w + lane%16 (the
-            // P_hi row for lane < 16, its P_lo twin above); the alpha of vector
-            // 16w + x lives in thread 4*(x%8), as its a (x < 8) or b value.
-            const int x = lane & 15;
-            const float al_a = __shfl_sync(0xffffffffu, alpha_a, 4 * (x & 7));
-            const float al_b = __shfl_sync(0xffffffffu, alpha_b, 4 * (x & 7));
-            const float al = (x < 8) ? al_a : al_b;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
-              uint32_t o[16];
-              tmem_ld16(tmem + C::kColO + lane_off + c0, o);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al);
-              tmem_st16(tmem + C::kColO + lane_off + c0, o);
-            }
-          }
-          if (i & 1) {
-            // P(i-1) *= alpha in place, hi and lo halves (rows ra, rb of
-            // this thread in both)
-            const uint32_t pc = tmem + C::kColS + ((i - 1) % kSBuf) * kT + lane_off;
-            scale_p_half(pc, alpha_a, alpha_b);
-            scale_p_half(pc + (16u << 16), alpha_a, alpha_b);
-          }
-        }
-        // P(i) replaces S(i) in its buffer: hi in lanes 32w+0..15, lo 16 above
         const uint32_t pcol = tmem + C::kColS + (i % kSBuf) * kT + lane_off;
         st_16x128b_x8_pair(pcol, pcol + (16u << 16), ph, pl);
       }
       tc_fence_before();
-      // one barrier per pair of buffers (a warp without query vectors may
-      // already be on the next pair while another still writes this one)
-      mbar_arrive(&mt.p_ready[(i >> 1) & 1]);
-      if ((i & 1) == 0 && i + 1 == n_tiles) mbar_arrive(&mt.p_ready[(i >> 1) & 1]);  // last tile without partner
+      mbar_arrive(&mt.p_ready[i % kSBuf]);
     }
     // ------------------------------------------------------ epilogue
-    const int last_pair = (n_tiles - 1) >> 1;
-    if (!ok || !mbar_wait(&mt.pv_done[last_pair & 1], (last_pair >> 1) & 1, wlim, abort_flag)) ok = false;
+    if (!ok || !mbar_wait(&mt.pv_done[(n_tiles - 1) % kSBuf], ((n_tiles - 1) / kSBuf) & 1, wlim, abort_flag))
+      ok = false;
     tc_fence_after();
     if (!ok) set_status(p.status, FP8KV_STATUS_TIMEOUT);
     if (warp_live) {
-      // O row of vector 16w + x: P_hi part in lane x, P_lo part in lane
-      // x + 16.  Per 64 columns the two lanes swap halves, so that lane x
-      // sums and stores columns 0..31 and lane x + 16 columns 32..63.
       const int myrow = 16 * warp + (lane & 15);
       const bool up = lane >= 16;
       float* dst = p.partial + (prow + myrow) * D + (up ? 32 : 0);

@@ -42,6 +42,7 @@ import math
 from dataclasses import dataclass, field
 from typing import Optional
 
+import numpy as np
 import torch
 
 E4M3_MAX = 448.0
@@ -121,6 +122,14 @@ def _gen(seed: int, *salt: int) -> torch.Generator:
     g = torch.Generator()
     g.manual_seed(_seed(seed, *salt))
     return g
+
+
+def _f32(x: float) -> float:
+    """x rounded to the nearest FP32 value.  The library's interface carries
+    softmax_scale, k_scale and v_scale as FP32, so every scale a problem holds
+    is an FP32 value: the oracle then computes with exactly the numbers the
+    kernels receive."""
+    return float(np.float32(x))
 
 
 def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
@@ -229,12 +238,12 @@ def make_dense(
                 continue
             kmax = max(kmax, float(draw(b, 0).abs().max()))
             vmax = max(vmax, float(draw(b, 1).abs().max()))
-        ks = kmax / FMT_MAX[kv_format] if kmax > 0 else 1.0
-        vs = vmax / FMT_MAX[kv_format] if vmax > 0 else 1.0
+        ks = _f32(kmax / FMT_MAX[kv_format]) if kmax > 0 else 1.0
+        vs = _f32(vmax / FMT_MAX[kv_format]) if vmax > 0 else 1.0
         q_k, q_v = ks, vs
     elif value_mode == "direct":
-        ks = float(k_scale)
-        vs = float(v_scale)
+        ks = _f32(k_scale)
+        vs = _f32(v_scale)
         q_k = q_v = 1.0
     else:
         raise ValueError(value_mode)
@@ -266,7 +275,7 @@ def make_dense(
     return Problem(
         name=name, mode="dense", B=B, q=q, Hq=Hq, Hkv=Hkv, D=D, page_size=page_size,
         q_fp16=q_fp16, k_cache=k_cache, v_cache=v_cache,
-        softmax_scale=float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
+        softmax_scale=_f32(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
         k_scale=float(ks), v_scale=float(vs), max_kv_len=max(lens) if lens else 0,
         block_table=block_table, row_len=rl,
         meta={"lens": lens, "seed": seed}, kv_format=kv_format,
@@ -317,8 +326,8 @@ def make_sparse(
 
     kmax = max(float(draw(b, 0).abs().max()) for b in range(B))
     vmax = max(float(draw(b, 1).abs().max()) for b in range(B))
-    ks = kmax / FMT_MAX[kv_format]
-    vs = vmax / FMT_MAX[kv_format]
+    ks = _f32(kmax / FMT_MAX[kv_format])
+    vs = _f32(vmax / FMT_MAX[kv_format])
     for b in range(B):
         ids = phys_of[b]
         k_cache[ids] = quantize_fp8(draw(b, 0), ks, kv_format).view(nmb, P, Hkv, D)
@@ -368,7 +377,7 @@ def make_sparse(
     return Problem(
         name=name, mode="sparse", B=B, q=q, Hq=Hq, Hkv=Hkv, D=D, page_size=P,
         q_fp16=q16, k_cache=k_cache, v_cache=v_cache,
-        softmax_scale=float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
+        softmax_scale=_f32(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
         k_scale=float(ks), v_scale=float(vs), max_kv_len=L,
         entry_tbl=entry_tbl, entry_mask=entry_mask, n_entries=n_entries,
         meta={"L": L, "topk_blocks": topk_blocks, "seed": seed,

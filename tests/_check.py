@@ -32,7 +32,13 @@ def ulp16(ref: np.ndarray) -> np.ndarray:
     return np.exp2(np.maximum(e, -14.0) - 10.0)
 
 
-def compare(gpu, ref, *, what="output", cond=None):
+def compare(gpu, ref, *, what="output", cond=None, max_floor_elements=None):
+    """Check gpu against ref (see the module docstring).
+
+    cond: apply the FP32 floor to every element.  max_floor_elements (with
+    cond): hold every element to the strict bound except at most this many,
+    which must still lie within the FP32-floor bound; their count is returned
+    as stats["floor_elements"]."""
     g = np.asarray(gpu, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     assert g.shape == r.shape, (g.shape, r.shape)
@@ -57,6 +63,12 @@ def compare(gpu, ref, *, what="output", cond=None):
         c = np.asarray(cond, dtype=np.float64)
         bound = MAX_ULPS * u + COND_U32 * 2.0 ** -24 * c
         stats["max_frac_of_bound"] = float((np.abs(diff) / bound).max()) if diff.size else 0.0
+        if max_floor_elements is not None:
+            floor = np.abs(diff) > MAX_ULPS * u
+            stats["floor_elements"] = int(floor.sum())
+            assert stats["floor_elements"] <= max_floor_elements, (
+                f"{what}: {stats['floor_elements']} elements beyond {MAX_ULPS} fp16 ulps "
+                f"(at most {max_floor_elements} may need the FP32 floor)")
     bad = np.abs(diff) > bound
     if bad.any():
         i = np.unravel_index(np.argmax(np.abs(diff) / bound), diff.shape)

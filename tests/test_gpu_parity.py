@@ -99,12 +99,18 @@ def test_poisoned_padding(name, poison):
 def test_c4_full():
     """64 independent decode requests (1.76 GB of cache, 1 % outliers x20):
     every query vector against the oracle, in the bench's launch config.  The
-    x20 outliers make some outputs cancel far below the size of their terms;
-    those elements are held to the FP32 forward-error floor (tests/_check.py)."""
+    x20 outliers make some outputs cancel far below the size of their terms.
+    The CUDA-core kernel keeps those resolvable with a two-part logit factor,
+    compensated sums across tiles and a compensated combine; every element is
+    held to the strict 4-ulp bound except at most one (measured: element
+    (0, 0, 7, 70), 4.45 ulps, |out| 8.8e-5 against cond 0.53, i.e. a
+    cancellation of ~6000x), which must lie within the FP32-state floor of
+    tests/_check.py: FP32 probabilities (exp2f is accurate to 2 ulps) cannot
+    resolve it further."""
     p = _problem("c4")
     dp = _dp(p)
     got = _run(dp)
-    stats = compare(got, _ref("c4"), what="c4", cond=oracle.attention_abs(p))
+    stats = compare(got, _ref("c4"), what="c4", cond=oracle.attention_abs(p), max_floor_elements=1)
     print("c4", stats)
     assert dp.status() == 0
 

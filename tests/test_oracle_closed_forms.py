@@ -28,7 +28,9 @@ def test_single_token_exact(orc):
     out = orc.attention(p)
     blk = int(p.block_table[0, 0])
     vbytes = p.v_cache[blk, 0, 0].tolist()
-    want = np.array([1.9 * _dec(b) for b in vbytes])
+    # the problem holds v_scale as the FP32 value the interface carries
+    assert p.v_scale == float(np.float32(1.9))
+    want = np.array([p.v_scale * _dec(b) for b in vbytes])
     assert np.array_equal(out[0, 0, 0], want)
     assert np.array_equal(out[0, 0, 1], want)
     assert np.all(out[0, 1] == 0.0) and not np.signbit(out[0, 1]).any()
@@ -58,7 +60,7 @@ def test_two_tokens_logistic(orc):
     for j in range(2):
         kb = p.k_cache[int(p.block_table[0, 0]), j, 0]
         kd = kb.view(torch.float8_e4m3fn).double().numpy()
-        kz.append(0.3 * p.k_scale * float(qv @ kd))
+        kz.append(p.softmax_scale * p.k_scale * float(qv @ kd))  # the FP32 scales the problem holds
     w1 = 1.0 / (1.0 + math.exp(kz[1] - kz[0]))
     assert len(w) == 2
     assert abs(w[0] - w1) < 1e-15 and abs(w[1] - (1 - w1)) < 1e-15
