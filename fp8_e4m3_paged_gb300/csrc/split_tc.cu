@@ -301,55 +301,63 @@ __device__ __forceinline__ TilePages fetch_pages(const Params& p, int b, int u0,
   return tp;
 }
 
-// Issue the bulk copies of one tile's K (or V) rows into a raw stage and
-// return the set of token slots that were copied.  Dense: runs of tokens
-// contiguous in a page; sparse: the tokens of each entry that some query row
-// attends (the tile's checked masks and microblock ids are in mk / bk).
-template <int D, int MODE>
-__device__ __forceinline__ uint64_t copy_rows(const Params& p, const uint8_t* cache, int64_t sb, int64_t st,
-                                              int64_t sh, int b, int g, int u0, int u1, int i, uint8_t* dst,
-                                              uint64_t* bar, const TilePages& tp, const uint32_t (&mk)[kE],
-                                              const int (&bk)[kE], bool report) {
+// Dense: issue the bulk copies of one tile's K (or V) rows into a raw stage
+// (one per run of tokens contiguous in a page) and return the set of token
+// slots that were copied.
+template <int D>
+__device__ __forceinline__ uint64_t copy_rows_dense(const Params& p, const uint8_t* cache, int64_t sb, int64_t st,
+                                                    int64_t sh, int b, int g, int u0, int u1, int i, uint8_t* dst,
+                                                    uint64_t* bar, const TilePages& tp, bool report) {
   uint64_t valid = 0ull;
-  if (MODE == FP8KV_MODE_DENSE) {
-    int t = 0;
-    while (t < kT) {
-      const int tok = u0 + i * kT + t;
-      if (tok >= u1) break;
-      const int page = tok / p.page_size, slot_in = tok % p.page_size;
-      const int dp = page - tp.page0;
-      const int blk = dp == 0 ? tp.blk[0] : dp == 1 ? tp.blk[1] : p.block_table[(int64_t)b * p.bt_stride + page];
-      const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
-      if (blk >= 0 && blk < p.num_kv_blocks) {
-        const uint8_t* src = cache + blk * sb + slot_in * st + g * sh;
-        // rows of consecutive slots are adjacent when the token stride is D
-        if (st == D) {
-          mbar_expect_tx(bar, run * D);
-          bulk_g2s(dst + t * D, src, run * D, bar);
-        } else {
-          for (int r = 0; r < run; ++r) {
-            mbar_expect_tx(bar, D);
-            bulk_g2s(dst + (t + r) * D, src + r * st, D, bar);
-          }
+  int t = 0;
+  while (t < kT) {
+    const int tok = u0 + i * kT + t;
+    if (tok >= u1) break;
+    const int page = tok / p.page_size, slot_in = tok % p.page_size;
+    const int dp = page - tp.page0;
+    const int blk = dp == 0 ? tp.blk[0] : dp == 1 ? tp.blk[1] : p.block_table[(int64_t)b * p.bt_stride + page];
+    const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
+    if (blk >= 0 && blk < p.num_kv_blocks) {
+      const uint8_t* src = cache + blk * sb + slot_in * st + g * sh;
+      // rows of consecutive slots are adjacent when the token stride is D
+      if (st == D) {
+        mbar_expect_tx(bar, run * D);
+        bulk_g2s(dst + t * D, src, run * D, bar);
+      } else {
+        for (int r = 0; r < run; ++r) {
+          mbar_expect_tx(bar, D);
+          bulk_g2s(dst + (t + r) * D, src + r * st, D, bar);
         }
-        valid |= ((run == 64) ? ~0ull : ((1ull << run) - 1ull)) << t;
-      } else if (report) {
-        set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
       }
-      t += run;
+      valid |= ((run == 64) ? ~0ull : ((1ull << run) - 1ull)) << t;
+    } else if (report) {
+      set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
     }
-  } else {
+    t += run;
+  }
+  return valid;
+}
+
+// Sparse, whole warp: token slot t of the tile is token t % 4 of entry t / 4
+// (whose checked mask and microblock id lane t / 4 holds); the slot is
+// copied only if some query row attends it.  Lane l issues slots l and l + 32;
+// returns the copied slots (the same value in every lane).
+template <int D>
+__device__ __forceinline__ uint64_t copy_tokens_sparse(const uint8_t* cache, int64_t sb, int64_t st, int64_t sh,
+                                                       int g, uint8_t* dst, uint64_t* bar, uint32_t mk, int bk,
+                                                       int lane) {
+  uint64_t valid = 0ull;
 #pragma unroll
-    for (int el = 0; el < kE; ++el) {
-      if (mk[el] == 0u) continue;
-      for (int tk = 0; tk < 4; ++tk) {
-        if ((mk[el] & (0x11111111u << tk)) == 0u) continue;
-        const int t = el * 4 + tk;
-        mbar_expect_tx(bar, D);
-        bulk_g2s(dst + t * D, cache + bk[el] * sb + tk * st + g * sh, D, bar);
-        valid |= 1ull << t;
-      }
+  for (int half = 0; half < 2; ++half) {
+    const int t = lane + 32 * half;
+    const uint32_t m = __shfl_sync(0xffffffffu, mk, t >> 2);
+    const int blk = __shfl_sync(0xffffffffu, bk, t >> 2);
+    const bool seen = (m & (0x11111111u << (t & 3))) != 0u;
+    if (seen) {
+      mbar_expect_tx(bar, D);
+      bulk_g2s(dst + t * D, cache + blk * sb + (t & 3) * st + g * sh, D, bar);
     }
+    valid |= (uint64_t)__ballot_sync(0xffffffffu, seen) << (32 * half);
   }
   return valid;
 }
@@ -570,76 +578,82 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 
   if (warp == kProdWarp || warp == kProdWarp + 1) {
     // ======================================================== producers
-    if (lane == 0) {
-      const bool is_k = warp == kProdWarp;
-      uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
-      uint64_t* raw_empty = is_k ? mt.rawk_empty : mt.rawv_empty;
-      uint64_t* valid = is_k ? mt.validk : mt.validv;
-      const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
-      const int64_t csb = is_k ? p.ksb : p.vsb, cst = is_k ? p.kst : p.vst, csh = is_k ? p.ksh : p.vsh;
-      uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
-      bool ok = true;
-      int issued = 0;  // tiles whose copies were issued
-      // the page walk of tile i + 1 (block ids, or sparse entries) is loaded
-      // while tile i waits for its stage
-      TilePages tp = {0, {-1, -1}};
-      uint32_t mk[kE];
-      int bk[kE];
-      auto fetch = [&](int i, TilePages& t, uint32_t (&m)[kE], int (&k)[kE]) {
-        if (MODE == FP8KV_MODE_DENSE) {
-          t = fetch_pages(p, b, u0, u1, i);
-        } else {
-#pragma unroll
-          for (int el = 0; el < kE; ++el) {
-            const int e = u0 + i * kE + el;
-            m[el] = (e < u1) ? p.entry_mask[(int64_t)b * p.entry_stride + e] : 0u;
-            k[el] = (e < u1) ? p.entry_tbl[(int64_t)b * p.entry_stride + e] : 0;
-          }
-        }
-      };
-      if (MODE == FP8KV_MODE_DENSE && u0 == u0_spec && u1 == u1_spec)
-        tp = tp_spec;
-      else
-        fetch(0, tp, mk, bk);
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const int slot = i % C::kRaw;
-        TilePages tp_next = {0, {-1, -1}};
-        uint32_t mk_next[kE];
-        int bk_next[kE];
-        if (i + 1 < n_tiles) fetch(i + 1, tp_next, mk_next, bk_next);
-        if (MODE == FP8KV_MODE_SPARSE_PAGE4) {
-          // an entry with a bad block contributes nothing
-#pragma unroll
-          for (int el = 0; el < kE; ++el) {
-            if (mk[el] != 0u && (bk[el] < 0 || bk[el] >= p.num_kv_blocks)) {
-              if (is_k) set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
-              mk[el] = 0u;
-            }
-          }
-        }
-        // the raw stage is free once the decoders loaded its previous tile
-        if (i >= C::kRaw && !mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag)) {
-          ok = false;
-          break;
-        }
-        valid[slot] = copy_rows<D, MODE>(p, cache, csb, cst, csh, b, g, u0, u1, i,
-                                         raw_base + slot * C::kRawBytes, &raw_full[slot], tp, mk, bk, is_k);
-        issued = i + 1;
-        if (is_k && i == 0 && (p.test_flags & FP8KV_TEST_STALL_PIPELINE)) {
+    // Dense: lane 0 walks the pages and issues one copy per run of tokens.
+    // Sparse: lane e holds entry e of the tile (mask and microblock id, loaded
+    // one tile ahead) and every lane issues the copies of two token slots.
+    const bool is_k = warp == kProdWarp;
+    uint64_t* raw_full = is_k ? mt.rawk_full : mt.rawv_full;
+    uint64_t* raw_empty = is_k ? mt.rawk_empty : mt.rawv_empty;
+    uint64_t* valid = is_k ? mt.validk : mt.validv;
+    const uint8_t* cache = is_k ? p.k_cache : p.v_cache;
+    const int64_t csb = is_k ? p.ksb : p.vsb, cst = is_k ? p.kst : p.vst, csh = is_k ? p.ksh : p.vsh;
+    uint8_t* raw_base = smem + (is_k ? C::kOffRawK : C::kOffRawV);
+    const bool stall_test = is_k && (p.test_flags & FP8KV_TEST_STALL_PIPELINE);
+    bool ok = true;
+    int issued = 0;  // tiles whose copies were issued
+    // the page walk of tile i + 1 (block ids, or sparse entries) is loaded
+    // while tile i waits for its stage
+    TilePages tp = {0, {-1, -1}};
+    uint32_t mk = 0u;
+    int bk = 0;
+    auto fetch = [&](int i, TilePages& t, uint32_t& m, int& k) {
+      if (MODE == FP8KV_MODE_DENSE) {
+        if (lane == 0) t = fetch_pages(p, b, u0, u1, i);
+      } else {
+        const int e = u0 + i * kE + lane;
+        const bool in = lane < kE && e < u1;
+        m = in ? p.entry_mask[(int64_t)b * p.entry_stride + e] : 0u;
+        k = in ? p.entry_tbl[(int64_t)b * p.entry_stride + e] : 0;
+      }
+    };
+    if (MODE == FP8KV_MODE_DENSE && u0 == u0_spec && u1 == u1_spec)
+      tp = tp_spec;
+    else
+      fetch(0, tp, mk, bk);
+    for (int i = 0; i < n_tiles; ++i) {
+      const int slot = i % C::kRaw;
+      TilePages tp_next = {0, {-1, -1}};
+      uint32_t mk_next = 0u;
+      int bk_next = 0;
+      if (i + 1 < n_tiles) fetch(i + 1, tp_next, mk_next, bk_next);
+      if (MODE == FP8KV_MODE_SPARSE_PAGE4 && mk != 0u && (bk < 0 || bk >= p.num_kv_blocks)) {
+        // an entry with a bad block contributes nothing
+        if (is_k) set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
+        mk = 0u;
+      }
+      // the raw stage is free once the decoders loaded its previous tile
+      bool got = true;
+      if (lane == 0 && i >= C::kRaw) got = mbar_wait(&raw_empty[slot], ((i / C::kRaw) - 1) & 1, wlim, abort_flag);
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
+        ok = false;
+        break;
+      }
+      uint64_t v = 0ull;
+      if (MODE == FP8KV_MODE_DENSE) {
+        if (lane == 0)
+          v = copy_rows_dense<D>(p, cache, csb, cst, csh, b, g, u0, u1, i, raw_base + slot * C::kRawBytes,
+                                 &raw_full[slot], tp, is_k);
+      } else {
+        v = copy_tokens_sparse<D>(cache, csb, cst, csh, g, raw_base + slot * C::kRawBytes, &raw_full[slot], mk, bk,
+                                  lane);
+      }
+      __syncwarp();  // every lane's expected bytes are registered before the arrival
+      issued = i + 1;
+      if (lane == 0) {
+        valid[slot] = v;
+        if (stall_test && i == 0) {
           // test only: hold back this arrival until a waiting warp has given
           // up, so that the timeout path runs; then stop issuing
           for (uint32_t k = 0; k < kDrainLimit && *abort_flag == 0u; ++k) __nanosleep(256);
-          mbar_arrive(&raw_full[slot]);
-          break;
         }
         mbar_arrive(&raw_full[slot]);
-        tp = tp_next;
-#pragma unroll
-        for (int el = 0; el < kE; ++el) {
-          mk[el] = mk_next[el];
-          bk[el] = bk_next[el];
-        }
       }
+      if (stall_test && i == 0) break;
+      tp = tp_next;
+      mk = mk_next;
+      bk = bk_next;
+    }
+    if (lane == 0) {
       // Drain: the copies of the last tile of every stage must have landed
       // before the CTA may exit (the decoders normally consumed them already;
       // after a give-up they may not have).  Nobody else arms these barriers,
