@@ -277,7 +277,8 @@ def run_ours(args):
         "config": {
             "workload": f"{args.workload}: {WORKLOAD_DESC.get(args.workload, '')}",
             "attended_kv_bytes_per_step": bytes_step,
-            "kernel": {1: "generic (CUDA cores)", 2: "tcgen05"}.get(dp.plan.kernel, str(dp.plan.kernel)),
+            "kernel": {1: "generic (CUDA cores)", 2: "tcgen05 (query rows)",
+                       3: "tcgen05 small group (tokens as rows)"}.get(dp.plan.kernel, str(dp.plan.kernel)),
             "num_splits": dp.plan.num_splits,
             "l2": f"inputs larger than L2: {copies} rotating KV copies, {copies * kv_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
             "launch": f"CUDA graphs of {copies} steps (one per KV copy), replayed back to back",

@@ -15,7 +15,7 @@ from typing import Optional
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8kv_attn.so")
 
-REVISION = 3
+REVISION = 4
 OK = 0
 EINVAL = -1
 EUNSUPPORTED = -2
@@ -32,6 +32,7 @@ KV_E5M2 = 1
 KERNEL_AUTO = 0
 KERNEL_GENERIC = 1
 KERNEL_TC = 2
+KERNEL_TC_SMALL = 3
 
 STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LEN = 0x2
@@ -60,7 +61,8 @@ class Plan(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("kv_format", ctypes.c_int32),
         ("test_flags", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 14),
+        ("min_part", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 13),
     ]
 
 

@@ -45,8 +45,10 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   if (d->page_size < 1 || d->max_kv_len < 0 || d->max_blocks < 0 || d->num_kv_blocks < 1)
     return FP8KV_EINVAL;
   if (d->num_sms < 0 || d->num_splits < 0) return FP8KV_EINVAL;
-  if (d->kernel < FP8KV_KERNEL_AUTO || d->kernel > FP8KV_KERNEL_TC) return FP8KV_EINVAL;
-  if (d->kernel == FP8KV_KERNEL_TC && d->head_dim != 128 && d->head_dim != 256) return FP8KV_EUNSUPPORTED;
+  if (d->kernel < FP8KV_KERNEL_AUTO || d->kernel > FP8KV_KERNEL_TC_SMALL) return FP8KV_EINVAL;
+  if ((d->kernel == FP8KV_KERNEL_TC || d->kernel == FP8KV_KERNEL_TC_SMALL) && d->head_dim != 128 &&
+      d->head_dim != 256)
+    return FP8KV_EUNSUPPORTED;
   if (d->kv_format != FP8KV_KV_E4M3 && d->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
   if (d->test_flags & ~FP8KV_TEST_STALL_PIPELINE) return FP8KV_EINVAL;
   if (d->mode == FP8KV_MODE_DENSE) {
@@ -83,18 +85,25 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   P.kv_format = d->kv_format;
   P.test_flags = d->test_flags;
 
-  // Kernel choice: the tcgen05 path when the grouped rows fill at least a
-  // quarter of its 64-row MMA tile and D is 128 or 256; otherwise the generic
-  // FP32 CUDA-core path (few rows per KV head: decode, small groups).
-  const bool tc = d->kernel == FP8KV_KERNEL_TC ||
-                  (d->kernel == FP8KV_KERNEL_AUTO && (P.head_dim == 128 || P.head_dim == 256) && P.rows >= 16);
+  // Kernel choice for D = 128 or 256: up to 16 query vectors per (request,
+  // KV head) -- decode and small verify groups -- the transposed tcgen05
+  // kernel (tokens as the MMA rows, so its softmax works on 128 tokens at a
+  // time whatever the group size); more, the tcgen05 kernel with the query
+  // vectors as the MMA rows (up to 64 per CTA).  D = 64: the FP32 CUDA-core
+  // kernel, which also serves every shape on request.
+  const bool tc_dims = P.head_dim == 128 || P.head_dim == 256;
+  int kind = d->kernel;
+  if (kind == FP8KV_KERNEL_AUTO)
+    kind = !tc_dims ? FP8KV_KERNEL_GENERIC : (P.rows <= kTcSmallRows ? FP8KV_KERNEL_TC_SMALL : FP8KV_KERNEL_TC);
   int tile, ctas_per_sm, max_part_tiles;
-  if (tc) {
-    P.kernel = kTc;
-    P.row_chunk = P.rows < kTcRows ? P.rows : kTcRows;
+  if (kind == FP8KV_KERNEL_TC || kind == FP8KV_KERNEL_TC_SMALL) {
+    const bool small = kind == FP8KV_KERNEL_TC_SMALL;
+    P.kernel = small ? kTcSmall : kTc;
+    const int cap = small ? kTcSmallRows : kTcRows;
+    P.row_chunk = P.rows < cap ? P.rows : cap;
     tile = kTcTileTokens;
     P.block_threads = kTcThreads;
-    P.smem_bytes = tc_smem_bytes(P.head_dim);
+    P.smem_bytes = tc_smem_bytes(P.head_dim, small);
     ctas_per_sm = 1;
     max_part_tiles = kTcMaxPartTiles;
   } else {
@@ -106,7 +115,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
     ctas_per_sm = 2;
     max_part_tiles = kGenericMaxPartTiles;
   }
-  if (P.test_flags && P.kernel != kTc) return FP8KV_EINVAL;  // the switch targets the pipeline waits
+  if (P.test_flags && P.kernel == kGeneric) return FP8KV_EINVAL;  // the switch targets the pipeline waits
   const int n_chunks = ceil_div(P.rows, P.row_chunk);
   P.tile_tokens = tile;
 
@@ -130,6 +139,12 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
     if (S < 1) S = 1;
   }
   P.num_splits = S;
+  // A batch with more (request, KV head, row chunk) units than the GPU has
+  // CTA slots is sized for its longest request; a partition of a short
+  // request is then kept at 16 tiles or more, so that few CTAs spend their
+  // fixed setup and pipeline fill on a tile or two (the rest exit at once).
+  const int unit_tokens = d->mode == FP8KV_MODE_DENSE ? tile : tile / 4;
+  P.min_part = units > (int64_t)ctas_per_sm * sms ? 16 * unit_tokens : 0;
   P.grid[0] = S;
   P.grid[1] = d->num_kv_heads * n_chunks;
   P.grid[2] = d->batch;
@@ -163,6 +178,7 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->num_kv_blocks = plan->num_kv_blocks;
   p->kv_format = plan->kv_format;
   p->test_flags = plan->test_flags;
+  p->min_part = plan->min_part;
   if (p->kv_format != FP8KV_KV_E4M3 && p->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
   if (p->G < 1 || p->rows != p->q_max * p->G || p->S < 1 || p->row_chunk < 1) return FP8KV_EINVAL;
 
@@ -229,7 +245,8 @@ extern "C" int fp8kv_attn_split(const fp8kv_attn_plan_t* plan, const fp8kv_attn_
   cudaError_t e;
   switch (plan->kernel) {
     case kGeneric: e = launch_split_generic(plan, p, reinterpret_cast<cudaStream_t>(stream)); break;
-    case kTc: e = launch_split_tc(plan, p, reinterpret_cast<cudaStream_t>(stream)); break;
+    case kTc:
+    case kTcSmall: e = launch_split_tc(plan, p, reinterpret_cast<cudaStream_t>(stream)); break;
     default: return FP8KV_EINVAL;
   }
   return e == cudaSuccess ? FP8KV_OK : FP8KV_ECUDA;

@@ -14,6 +14,7 @@ namespace fp8kv {
 enum Kernel : int32_t {
   kGeneric = FP8KV_KERNEL_GENERIC,  // CUDA-core FP32 path, any supported shape
   kTc = FP8KV_KERNEL_TC,            // tcgen05 tensor-core path (head_dim 128/256)
+  kTcSmall = FP8KV_KERNEL_TC_SMALL, // tcgen05, transposed for row groups of at most 16 (decode)
 };
 
 constexpr int kGenericThreads = 256;
@@ -28,6 +29,7 @@ struct Params {
   int32_t page_size, max_kv_len, max_blocks, num_kv_blocks;
   int32_t kv_format;  // FP8KV_KV_E4M3 or FP8KV_KV_E5M2
   int32_t test_flags; // FP8KV_TEST_* (0 in production)
+  int32_t min_part;   // shortest partition: tokens (dense) or entries (sparse), 0 = none
   // inputs
   const uint16_t* q;
   const uint8_t* k_cache;
@@ -57,6 +59,7 @@ int build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a, Params
 
 cudaError_t launch_split_generic(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_split_tc(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
+cudaError_t launch_split_tc_small(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_combine(const fp8kv_attn_plan_t* plan, const Params& p, cudaStream_t s);
 cudaError_t launch_cache_write(const fp8kv_cache_write_args& a, cudaStream_t s);
 cudaError_t launch_merge(const fp8kv_merge_args& a, int32_t scale_rank, cudaStream_t s);
@@ -82,7 +85,8 @@ struct DeviceOnce {
 int generic_smem_bytes(int D, int row_chunk);
 
 // Tensor-core path: shared-memory bytes (D = 128 or 256), threads, tile size.
-int tc_smem_bytes(int D);
+int tc_smem_bytes(int D, bool small_group);
+constexpr int kTcSmallRows = 16;     // query vectors per CTA of the small-group kernel
 constexpr int kTcThreads = 480;
 constexpr int kTcTileTokens = 64;
 constexpr int kTcRows = 64;

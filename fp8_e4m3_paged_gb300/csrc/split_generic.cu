@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
     }
   }
   const int unit = (MODE == FP8KV_MODE_DENSE) ? TT : TT / 4;  // tokens or entries per tile
-  int per = (U + p.S - 1) / p.S;
+  int per = max((U + p.S - 1) / p.S, p.min_part);
   per = (per + unit - 1) / unit * unit;
   const int u0 = s * per;
   const int u1 = min(U, u0 + per);

@@ -82,7 +82,8 @@ extern "C" int fp8kv_attn_forward_static(const fp8kv_attn_plan_t* plan, const fp
   cudaError_t e;
   switch (plan->kernel) {
     case kGeneric: e = launch_split_generic(plan, p, st); break;
-    case kTc: e = launch_split_tc(plan, p, st); break;
+    case kTc:
+    case kTcSmall: e = launch_split_tc(plan, p, st); break;
     default: return FP8KV_EINVAL;
   }
   if (e != cudaSuccess) return FP8KV_ECUDA;

@@ -69,7 +69,7 @@ extern "C" {
  * stale plan cannot reach kernels with another partial layout ("DFlash2 E4M3
  * attention with FP32 state", intro paragraph 5: the wrapper requires a given
  * precision capability revision). */
-#define FP8KV_ATTN_REVISION 3
+#define FP8KV_ATTN_REVISION 4
 
 /* Return codes. */
 #define FP8KV_OK 0
@@ -94,6 +94,8 @@ extern "C" {
 #define FP8KV_KERNEL_AUTO 0
 #define FP8KV_KERNEL_GENERIC 1 /* FP32 CUDA-core path: every supported shape */
 #define FP8KV_KERNEL_TC 2      /* tcgen05 tensor-core path: head_dim 128/256 (else FP8KV_EUNSUPPORTED) */
+#define FP8KV_KERNEL_TC_SMALL 3 /* tcgen05, transposed (tokens as the MMA rows, at most 16 query vectors
+                                   per CTA): decode-sized groups; head_dim 128/256 */
 
 /* Sticky device status bits (workspace word at byte offset 0). */
 #define FP8KV_STATUS_BAD_BLOCK 0x1   /* block / microblock id outside [0, num_kv_blocks) */
@@ -153,7 +155,8 @@ typedef struct {
   int64_t workspace_bytes; /* minimum workspace size */
   int32_t kv_format;       /* FP8KV_KV_* of the cache bytes */
   int32_t test_flags;      /* FP8KV_TEST_* (0 in production) */
-  int32_t reserved[14];
+  int32_t min_part;        /* shortest non-empty partition: tokens (dense) or entries (sparse) */
+  int32_t reserved[13];
 } fp8kv_attn_plan_t;
 
 /* Per-call arguments.  All pointers are device pointers owned by the caller,

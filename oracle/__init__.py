@@ -36,6 +36,11 @@ Parity status of each exported function (what pins it, in ``tests/``):
   row_weights         sum to 1, two-token logistic closed form
   attention_abs       equals attention when every V byte is non-negative;
                       bounds |attention| elementwise
+  attention_logit_cond
+                      two-token closed form w1 w2 (a1 + a2) |v1 - v2|, zero
+                      for one token and for equal values, and a bound on
+                      the measured output change under relative logit
+                      perturbations (k_scale scaled by 1 +- eps)
 """
 
 from __future__ import annotations
@@ -112,6 +117,7 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.orc_attention_items.argtypes = [P, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_split.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_abs.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
+    lib.orc_attention_logit_cond.argtypes = [P, ctypes.c_void_p, ctypes.c_int]
     lib.orc_row_weights.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
     lib.orc_attention_lse.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.orc_merge.restype = None
@@ -225,6 +231,18 @@ def attention_abs(p, threads: Optional[int] = None, plant: int = 0, **over) -> n
     pin = _Pinned(p, **over)
     out = np.zeros((p.B, p.q, p.Hq, p.D), dtype=np.float64)
     rc = load(plant).orc_attention_abs(ctypes.byref(pin.s), out.ctypes.data, threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle rejected the problem")
+    return out
+
+
+def attention_logit_cond(p, threads: Optional[int] = None, plant: int = 0, **over) -> np.ndarray:
+    """Per-element logit condition sum_j w_j a_j |v_j[d] - out[d]| ([B][q][Hq][D]),
+    a_j = |softmax_scale k_scale| sum_d |q[d] dec(K_j[d])|: logit errors
+    |dz_j| <= eps a_j move the output by at most eps times this (first order)."""
+    pin = _Pinned(p, **over)
+    out = np.zeros((p.B, p.q, p.Hq, p.D), dtype=np.float64)
+    rc = load(plant).orc_attention_logit_cond(ctypes.byref(pin.s), out.ctypes.data, threads or default_threads())
     if rc != 0:
         raise ValueError("oracle rejected the problem")
     return out

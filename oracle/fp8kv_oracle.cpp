@@ -335,6 +335,44 @@ static void row_head_abs(const orc_problem* p, int b, int r, int h, double* out)
   for (int d = 0; d < D; ++d) out[d] = std::fabs(p->v_scale) * acc[d];
 }
 
+// Logit condition of each output element:
+//   sum_j w_j a_j |v_scale dec(V_j[d]) - out[d]|,
+//   a_j = |softmax_scale k_scale| sum_d' |q[d'] dec(K_j[d'])|.
+// If every logit z_j carries an absolute error |dz_j| <= eps a_j (the a
+// priori bound of a dot product evaluated in floating point is a small
+// multiple of the unit roundoff times the sum of |products|), the softmax
+// weights move by dw_j = w_j (dz_j - sum_k w_k dz_k), so the output moves by
+// sum_j w_j dz_j (v_j - out) to first order: at most eps times this value.
+static void row_head_logit_cond(const orc_problem* p, int b, int r, int h, double* out) {
+  const int D = p->D;
+  std::vector<Tok> toks;
+  visible(p, b, r, group_of(p, h), toks);
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  if (toks.empty()) return;
+  std::vector<double> z;
+  logits(p, b, r, h, toks, z);
+  double M = -std::numeric_limits<double>::infinity();
+  for (double v : z) M = std::max(M, v);
+  double S = 0.0;
+  for (double v : z) S += std::exp(v - M);
+  const uint16_t* qv = p->q_bits + (((int64_t)b * p->q + r) * p->Hq + h) * D;
+  const double sc = std::fabs(p->softmax_scale * p->k_scale);
+  std::vector<double> w(toks.size()), a(toks.size()), o(D, 0.0);
+  for (size_t j = 0; j < toks.size(); ++j) {
+    w[j] = std::exp(z[j] - M) / S;
+    const uint8_t* kb = p->k_cache + toks[j].k_off;
+    double s = 0.0;
+    for (int d = 0; d < D; ++d) s += std::fabs(orc_f16(qv[d]) * dec(p, kb[d]));
+    a[j] = sc * s;
+    const uint8_t* vb = p->v_cache + toks[j].v_off;
+    for (int d = 0; d < D; ++d) o[d] += w[j] * p->v_scale * dec(p, vb[d]);
+  }
+  for (size_t j = 0; j < toks.size(); ++j) {
+    const uint8_t* vb = p->v_cache + toks[j].v_off;
+    for (int d = 0; d < D; ++d) out[d] += w[j] * a[j] * std::fabs(p->v_scale * dec(p, vb[d]) - o[d]);
+  }
+}
+
 static void row_head(const orc_problem* p, int b, int r, int h, double* out) {
   const int D = p->D;
   std::vector<Tok> toks;
@@ -467,6 +505,19 @@ ORC_API int orc_attention_abs(const orc_problem* p, double* out, int nthreads) {
     const int r = (int)((i / p->Hq) % p->q);
     const int b = (int)(i / ((int64_t)p->Hq * p->q));
     row_head_abs(p, b, r, h, out + i * p->D);
+  });
+  return 0;
+}
+
+// out: [B][q][Hq][D] doubles, the logit condition of row_head_logit_cond.
+ORC_API int orc_attention_logit_cond(const orc_problem* p, double* out, int nthreads) {
+  if (check(p)) return -1;
+  const int64_t n = (int64_t)p->B * p->q * p->Hq;
+  parallel_items(n, nthreads, [&](int64_t i) {
+    const int h = (int)(i % p->Hq);
+    const int r = (int)((i / p->Hq) % p->q);
+    const int b = (int)(i / ((int64_t)p->Hq * p->q));
+    row_head_logit_cond(p, b, r, h, out + i * p->D);
   });
   return 0;
 }

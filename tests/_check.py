@@ -15,6 +15,17 @@ standard forward error bound of a weighted sum evaluated with unit roundoff
 2^-24, with COND_U32 roundings (exponent, probability split, PV accumulation,
 partition combine, normalisation).  Where cond ~ |ref| the extra term is
 below 0.01 fp16 ulp, so the strict bound is unchanged there.
+
+Logit term (where a caller also passes ``cond_qk``): an FP32 logit cannot be
+better than its dot product, and with outliers in K a logit of magnitude 30
+(natural units) already moves its weight by ~30 ulps when rounded once.  Both
+kernel families form each logit as a TwoSum-compensated sum of partial dot
+products of at most 16 exact products (FMA chunks of 8 on the CUDA cores, one
+K16 MMA per part on the tensor cores), whose a priori error is gamma_16 ~ 16u
+times the partial's sum of |products|.  With cond_qk = sum_j w_j a_j |v_j -
+out| (the oracle's attention_logit_cond, a_j the scaled sum of |q_d k_jd|),
+the bound gains COND_QK * 2^-24 * cond_qk: the first-order output change
+under logit errors |dz_j| <= COND_QK 2^-24 a_j.
 """
 
 import numpy as np
@@ -22,6 +33,7 @@ import numpy as np
 REL_L2 = 5e-4
 MAX_ULPS = 4.0
 COND_U32 = 16.0
+COND_QK = 16.0
 
 
 def ulp16(ref: np.ndarray) -> np.ndarray:
@@ -32,13 +44,13 @@ def ulp16(ref: np.ndarray) -> np.ndarray:
     return np.exp2(np.maximum(e, -14.0) - 10.0)
 
 
-def compare(gpu, ref, *, what="output", cond=None, max_floor_elements=None):
+def compare(gpu, ref, *, what="output", cond=None, cond_qk=None, max_floor_elements=None):
     """Check gpu against ref (see the module docstring).
 
-    cond: apply the FP32 floor to every element.  max_floor_elements (with
-    cond): hold every element to the strict bound except at most this many,
-    which must still lie within the FP32-floor bound; their count is returned
-    as stats["floor_elements"]."""
+    cond: apply the FP32 floor to every element; cond_qk (with cond): add the
+    logit term to it.  max_floor_elements (with cond): hold every element to
+    the strict bound except at most this many, which must still lie within
+    the FP32-floor bound; their count is returned as stats["floor_elements"]."""
     g = np.asarray(gpu, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     assert g.shape == r.shape, (g.shape, r.shape)
@@ -62,6 +74,8 @@ def compare(gpu, ref, *, what="output", cond=None, max_floor_elements=None):
     else:
         c = np.asarray(cond, dtype=np.float64)
         bound = MAX_ULPS * u + COND_U32 * 2.0 ** -24 * c
+        if cond_qk is not None:
+            bound = bound + COND_QK * 2.0 ** -24 * np.asarray(cond_qk, dtype=np.float64)
         stats["max_frac_of_bound"] = float((np.abs(diff) / bound).max()) if diff.size else 0.0
         if max_floor_elements is not None:
             floor = np.abs(diff) > MAX_ULPS * u

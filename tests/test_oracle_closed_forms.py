@@ -105,3 +105,69 @@ def test_abs_condition(orc):
     p.v_cache &= 0x7F
     p.v_cache[p.v_cache == 0x7F] = 0x7E
     assert np.array_equal(orc.attention_abs(p), orc.attention(p))
+
+
+def _kv_rows(p, b, g, n):
+    rows_k, rows_v = [], []
+    for j in range(n):
+        blk = int(p.block_table[b, j // p.page_size])
+        rows_k.append(p.k_cache[blk, j % p.page_size, g].view(torch.float8_e4m3fn).double().numpy())
+        rows_v.append(p.v_cache[blk, j % p.page_size, g].view(torch.float8_e4m3fn).double().numpy())
+    return rows_k, rows_v
+
+
+def test_logit_cond_two_tokens(orc):
+    """Two tokens: v_1 - out = w_2 (v_1 - v_2) and v_2 - out = w_1 (v_2 - v_1),
+    so the condition is w_1 w_2 (a_1 + a_2) |v_1 - v_2| with a_j the scaled
+    sum of |q_d k_jd|."""
+    p = make_dense(B=1, q=1, Hq=1, Hkv=1, D=8, page_size=2, lens=[2], seed=18, softmax_scale=0.3)
+    cnd = orc.attention_logit_cond(p)[0, 0, 0]
+    ks, vs = _kv_rows(p, 0, 0, 2)
+    qv = p.q_fp16[0, 0, 0].double().numpy()
+    sc = p.softmax_scale * p.k_scale
+    z = [sc * float(qv @ k) for k in ks]
+    w1 = 1.0 / (1.0 + math.exp(z[1] - z[0]))
+    w2 = 1.0 - w1
+    a = [sc * float(np.abs(qv * k).sum()) for k in ks]
+    want = w1 * w2 * (a[0] + a[1]) * np.abs(p.v_scale * (vs[0] - vs[1]))
+    np.testing.assert_allclose(cnd, want, rtol=1e-12, atol=0)
+    assert (cnd > 0).any()
+
+
+def test_logit_cond_zero_cases(orc):
+    # one visible token: out = v_1 exactly, whatever its logit
+    p = make_dense(B=1, q=2, Hq=2, Hkv=1, D=8, page_size=4, lens=[6], seed=19, row_len=[[1, 0]])
+    c = orc.attention_logit_cond(p)
+    assert np.all(c == 0.0)
+    # identical V rows: every v_j equals the output
+    p = make_dense(B=1, q=1, Hq=1, Hkv=1, D=16, page_size=5, lens=[13], seed=20)
+    v0 = p.v_cache[int(p.block_table[0, 0]), 0, 0].clone()
+    for j in range(13):
+        p.v_cache[int(p.block_table[0, j // 5]), j % 5, 0] = v0
+    # zero up to the FP64 rounding of out = sum_j w_j v_0 (weights summing to 1)
+    ks, _ = _kv_rows(p, 0, 0, 13)
+    qv = p.q_fp16[0, 0, 0].double().numpy()
+    amax = p.softmax_scale * p.k_scale * max(float(np.abs(qv * k).sum()) for k in ks)
+    assert np.all(orc.attention_logit_cond(p) <= 1e-14 * amax * orc.attention_abs(p))
+
+
+def test_logit_cond_bounds_logit_perturbation(orc):
+    """Scaling k_scale by (1 + eps) perturbs every logit by eps z_j, |eps z_j| <=
+    eps a_j: the output change stays within eps times the condition, and comes
+    close to it somewhere (the bound is attained up to sign patterns)."""
+    import copy
+    p = make_dense(B=2, q=2, Hq=4, Hkv=2, D=32, page_size=8, lens=[150, 77], seed=21,
+                   value_mode="direct", k_scale=0.75, v_scale=1.25, softmax_scale=0.5)
+    base = orc.attention(p)
+    cnd = orc.attention_logit_cond(p)
+    ab = orc.attention_abs(p)
+    ratios = []
+    for f in (1 + 2.0 ** -20, 1 - 2.0 ** -20):
+        p2 = copy.copy(p)
+        p2.k_scale = p.k_scale * f
+        eps = abs(p2.k_scale / p.k_scale - 1.0)
+        d = np.abs(orc.attention(p2) - base)
+        assert np.all(d <= eps * cnd * (1 + 1e-3) + 1e-13 * ab)
+        live = cnd > 0
+        ratios.append(float((d[live] / (eps * cnd[live])).max()))
+    assert max(ratios) > 0.3, ratios
