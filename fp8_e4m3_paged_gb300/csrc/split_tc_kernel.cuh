@@ -264,8 +264,9 @@ __device__ __forceinline__ uint4 dec8(uint32_t a, uint32_t b) {
 // a compile-time offset.  It runs in two steps: load_raw brings the thread's
 // raw chunks into registers (after which the raw stage may be refilled), and
 // store_tile converts and stores them.  Rows whose bit in `valid` is clear
-// were not copied and become zeros.  With CHECK (the V stream) a non-finite
-// code is written as 0 and `bad` is set (see the kernel's header).
+// were not copied and become zeros.  zap_nonfinite_tile (the V stream, in
+// between) writes non-finite codes as 0 and sets `bad` (see the kernel's
+// header).
 template <int D>
 struct DecShape {
   static constexpr int kChunks = D / 16;           // 16-byte raw chunks per row
@@ -274,9 +275,8 @@ struct DecShape {
   static_assert(kDecThreads % kChunks == 0 && kT % kR == 0, "decoder shape");
 };
 
-template <int D, int FMT, bool CHECK>
-__device__ __forceinline__ void load_raw(const uint8_t* raw, uint64_t valid, int lt, uint4 (&w)[DecShape<D>::kPer],
-                                         bool& bad) {
+template <int D>
+__device__ __forceinline__ void load_raw(const uint8_t* raw, uint64_t valid, int lt, uint4 (&w)[DecShape<D>::kPer]) {
   using S = DecShape<D>;
   const int c = lt % S::kChunks, t0 = lt / S::kChunks;
   const uint8_t* src = raw + t0 * D + c * 16;
@@ -286,16 +286,25 @@ __device__ __forceinline__ void load_raw(const uint8_t* raw, uint64_t valid, int
     w[k] = (full || ((valid >> (t0 + k * S::kR)) & 1ull)) ? *reinterpret_cast<const uint4*>(src + k * S::kR * D)
                                                          : make_uint4(0, 0, 0, 0);
   }
-  if (CHECK) {
+}
+
+// One test over the thread's chunks (no branch per chunk: on the V path a
+// branch per chunk cost ~4 us of a 128K-token split), then the rare rewrite.
+template <int D, int FMT>
+__device__ __forceinline__ void zap_nonfinite_tile(uint4 (&w)[DecShape<D>::kPer], bool& bad) {
+  using S = DecShape<D>;
+  constexpr bool e5 = FMT == FP8KV_KV_E5M2;
+  uint32_t any = 0u;
+#pragma unroll
+  for (int k = 0; k < S::kPer; ++k) any |= nonfinite_codes(w[k], e5);
+  if (any != 0u) {
+    bad = true;
 #pragma unroll
     for (int k = 0; k < S::kPer; ++k) {
-      if (nonfinite_codes(w[k], FMT == FP8KV_KV_E5M2) != 0u) {
-        bad = true;
-        w[k].x = zap_nonfinite(w[k].x, FMT == FP8KV_KV_E5M2);
-        w[k].y = zap_nonfinite(w[k].y, FMT == FP8KV_KV_E5M2);
-        w[k].z = zap_nonfinite(w[k].z, FMT == FP8KV_KV_E5M2);
-        w[k].w = zap_nonfinite(w[k].w, FMT == FP8KV_KV_E5M2);
-      }
+      w[k].x = zap_nonfinite(w[k].x, e5);
+      w[k].y = zap_nonfinite(w[k].y, e5);
+      w[k].z = zap_nonfinite(w[k].z, e5);
+      w[k].w = zap_nonfinite(w[k].w, e5);
     }
   }
 }
@@ -768,11 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
         break;
       }
       uint4 w[DecShape<D>::kPer];
-      if (is_k)
-        load_raw<D, FMT, false>(raw_base + slot * C::kRawBytes, valid[slot], lt, w, bad);
-      else
-        load_raw<D, FMT, true>(raw_base + slot * C::kRawBytes, valid[slot], lt, w, bad);
+      load_raw<D>(raw_base + slot * C::kRawBytes, valid[slot], lt, w);
       mbar_arrive(&raw_empty[slot]);
+      // V: the check runs after the raw stage is handed back, off the paths
+      // of both the refill and the PV (placed before the hand-back it cost
+      // ~1.5 us more, after the wait for the operand stage ~3 us more)
+      if (!is_k) zap_nonfinite_tile<D, FMT>(w, bad);
       if (is_k) {
         // K stages hold pairs of tiles interleaved per 64-column block, so
         // that two consecutive tiles form one 128-row operand of the pair's
