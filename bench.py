@@ -399,9 +399,9 @@ def _item_tokens(p):
                     items.append((b, r, h))
                     toks.append(n)
     else:
-        from synth.workloads import masks_u32
+        from synth.workloads import masks_u64
 
-        m = masks_u32(p)
+        m = masks_u64(p)
         for b in range(p.B):
             mb = m[b, :int(p.n_entries[b])]
             for r in range(p.q):

@@ -15,7 +15,7 @@ from typing import Optional
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8kv_attn.so")
 
-REVISION = 4
+REVISION = 5
 OK = 0
 EINVAL = -1
 EUNSUPPORTED = -2
@@ -82,6 +82,7 @@ class Args(ctypes.Structure):
         ("k_scale_dev", ctypes.c_void_p), ("v_scale_dev", ctypes.c_void_p),
         ("out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("entry_mask_hi", ctypes.c_void_p),
     ]
 
 
@@ -127,6 +128,7 @@ class SelectArgs(ctypes.Structure):
         ("sel", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int64),
         ("entry_tbl", ctypes.c_void_p), ("entry_mask", ctypes.c_void_p), ("entry_stride", ctypes.c_int64),
         ("n_entries", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("entry_mask_hi", ctypes.c_void_p),
     ]
 
 
@@ -222,7 +224,7 @@ def make_args(*, q, k_cache, v_cache, out, workspace, softmax_scale: float,
               k_scale: float = 1.0, v_scale: float = 1.0,
               block_table=None, row_kv_len=None,
               entry_tbl=None, entry_mask=None, n_entries=None,
-              k_scale_dev=None, v_scale_dev=None) -> Args:
+              k_scale_dev=None, v_scale_dev=None, entry_mask_hi=None) -> Args:
     """Fill an Args struct from torch CUDA tensors.
 
     k_cache / v_cache: uint8 tensors indexed [block][slot][kv_head][d] (any
@@ -247,6 +249,7 @@ def make_args(*, q, k_cache, v_cache, out, workspace, softmax_scale: float,
         a.entry_tbl = _ptr(entry_tbl)
         a.entry_stride = entry_tbl.stride(0)
     a.entry_mask = _ptr(entry_mask)
+    a.entry_mask_hi = _ptr(entry_mask_hi)
     a.n_entries = _ptr(n_entries)
     a.softmax_scale = float(softmax_scale)
     a.k_scale = float(k_scale)
@@ -345,10 +348,11 @@ def fp8kv_attn_merge_scale(args: MergeArgs, rank: int, stream: int = 0) -> None:
 
 
 def make_select_args(*, sel, block_table, max_blocks: int, null_block: int, entry_tbl, entry_mask,
-                     n_entries, status=None) -> SelectArgs:
+                     n_entries, status=None, entry_mask_hi=None) -> SelectArgs:
     """sel: int32 [B][q][topk]; block_table: int32 [B][>= max_blocks];
-    entry_tbl / entry_mask: int32 [B][stride] (the mask tensor holds the
-    uint32 bit patterns); n_entries: int32 [B] (torch CUDA tensors)."""
+    entry_tbl / entry_mask (/ entry_mask_hi for q > 8): int32 [B][stride]
+    (the mask tensors hold the uint32 bit patterns); n_entries: int32 [B]
+    (torch CUDA tensors)."""
     a = SelectArgs()
     a.batch, a.q_max, a.topk = sel.shape
     a.max_blocks, a.null_block = max_blocks, null_block
@@ -356,6 +360,7 @@ def make_select_args(*, sel, block_table, max_blocks: int, null_block: int, entr
     a.block_table, a.block_table_stride = _ptr(block_table), block_table.stride(0)
     a.entry_tbl, a.entry_mask, a.entry_stride = _ptr(entry_tbl), _ptr(entry_mask), entry_tbl.stride(0)
     a.n_entries, a.status = _ptr(n_entries), _ptr(status)
+    a.entry_mask_hi = _ptr(entry_mask_hi)
     return a
 
 

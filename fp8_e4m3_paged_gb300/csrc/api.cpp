@@ -54,7 +54,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   if (d->mode == FP8KV_MODE_DENSE) {
     if ((int64_t)d->max_blocks * d->page_size < d->max_kv_len) return FP8KV_EINVAL;
   } else {
-    if (d->page_size != 4 || d->q_max > 8) return FP8KV_EUNSUPPORTED;
+    if (d->page_size != 4) return FP8KV_EUNSUPPORTED;  // q_max <= 16: two mask words above 8 rows
   }
 
   int sms = d->num_sms;
@@ -201,6 +201,7 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
     if (a->block_table_stride < plan->max_blocks || a->block_table_stride < 1) return FP8KV_EINVAL;
   } else {
     if (!a->entry_tbl || !a->entry_mask || !a->n_entries) return FP8KV_EINVAL;
+    if (plan->q_max > 8 && !a->entry_mask_hi) return FP8KV_EINVAL;  // rows 8..15 need the second words
     if (a->entry_stride < plan->max_blocks || a->entry_stride < 1) return FP8KV_EINVAL;
   }
   if (!std::isfinite(a->softmax_scale)) return FP8KV_EINVAL;
@@ -221,6 +222,7 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->row_len = a->row_kv_len;
   p->entry_tbl = a->entry_tbl;
   p->entry_mask = a->entry_mask;
+  p->entry_mask_hi = plan->q_max > 8 ? a->entry_mask_hi : nullptr;
   p->n_entries = a->n_entries;
   p->entry_stride = a->entry_stride;
   p->softmax_scale = a->softmax_scale;
@@ -332,7 +334,8 @@ extern "C" int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, f
 
 extern "C" int fp8kv_attn_select_to_entries(const fp8kv_select_args* a, fp8kv_stream_t stream) {
   if (!a) return FP8KV_EINVAL;
-  if (a->batch < 0 || a->q_max < 1 || a->q_max > 8 || a->topk < 0 || a->max_blocks < 1) return FP8KV_EINVAL;
+  if (a->batch < 0 || a->q_max < 1 || a->q_max > 16 || a->topk < 0 || a->max_blocks < 1) return FP8KV_EINVAL;
+  if (a->q_max > 8 && !a->entry_mask_hi) return FP8KV_EINVAL;
   if (a->block_table_stride < a->max_blocks) return FP8KV_EINVAL;
   const int64_t cap = ((int64_t)a->q_max * a->topk + 7) / 8 * 8;
   if (a->entry_stride < cap || a->entry_stride < 1) return FP8KV_EINVAL;

@@ -72,6 +72,17 @@ __device__ __forceinline__ uint32_t zap_nonfinite(uint32_t x, bool e5m2) {
   return x & ~((top >> 7) * 0xFFu);
 }
 
+// Sparse visibility: query row r sees token t of an entry iff bit 4r + t of
+// its mask word (rows 0..7) or bit 4(r - 8) + t of its second word (rows
+// 8..15, absent with 8 or fewer rows) is set.
+__device__ __forceinline__ uint32_t sparse_bit(uint32_t lo, uint32_t hi, int r, int t) {
+  return ((r < 8 ? lo : hi) >> (4 * (r & 7) + t)) & 1u;
+}
+// The second mask word of entry e of request b (0 without one).
+__device__ __forceinline__ uint32_t mask_hi_of(const uint32_t* mask_hi, int64_t stride, int b, int e) {
+  return mask_hi ? mask_hi[(int64_t)b * stride + e] : 0u;
+}
+
 __device__ __forceinline__ void set_status(unsigned int* status, unsigned int bit) {
   atomicOr(status, bit);
 }

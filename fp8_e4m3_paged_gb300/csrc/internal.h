@@ -40,6 +40,7 @@ struct Params {
   const int32_t* row_len;
   const int32_t* entry_tbl;
   const uint32_t* entry_mask;
+  const uint32_t* entry_mask_hi;  // sparse rows 8..15 (NULL with q_max <= 8)
   const int32_t* n_entries;
   int64_t entry_stride;
   // scales: logit factor = softmax_scale * k_scale * log2(e)

@@ -44,7 +44,7 @@ __host__ __device__ inline GenericSmem generic_layout(int D, int RC) {
   L.p = off;     off += TT * (RC + 1);   // Ps[t][row] (padded rows)
   L.alpha = off; off += RC;              // per-row rescale factor of this tile
   L.nrow = off;  off += RC;              // per-row live length (int) / row index
-  L.mask = off;  off += 8;               // sparse: this tile's 8 masks (uint)
+  L.mask = off;  off += 16;              // sparse: this tile's 8 masks, then their second words (uint)
   L.total_bytes = off * 4;
   return L;
 }
@@ -165,16 +165,18 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
     constexpr int VPT = D / 16;
     if (MODE == FP8KV_MODE_SPARSE_PAGE4 && tid < 8) {
       const int e = tb + tid;
-      uint32_t mk = 0;
+      uint32_t mk = 0, mkh = 0;
       if (e < u1) {
         mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
+        mkh = mask_hi_of(p.entry_mask_hi, p.entry_stride, b, e);
         const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-        if (mk != 0u && (blk < 0 || blk >= p.num_kv_blocks)) {
+        if ((mk | mkh) != 0u && (blk < 0 || blk >= p.num_kv_blocks)) {
           set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
-          mk = 0;
+          mk = mkh = 0;
         }
       }
       Msk[tid] = mk;
+      Msk[8 + tid] = mkh;
     }
     if (MODE == FP8KV_MODE_SPARSE_PAGE4) __syncthreads();
     for (int idx = tid; idx < TT * VPT; idx += NT) {
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
         }
       } else {
         const int e = tb + t / 4, tk = t % 4;
-        const uint32_t mk = Msk[t / 4];
+        const uint32_t mk = Msk[t / 4] | Msk[8 + t / 4];
         // only tokens that at least one query row attends are read
         if (e < u1 && (mk & (0x11111111u << tk)) != 0u) {
           const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
       const int t = lane;
       const int tok = tb + ((MODE == FP8KV_MODE_DENSE) ? t : t / 4);
       const uint32_t mk = (MODE == FP8KV_MODE_DENSE) ? 0u : Msk[t / 4];
+      const uint32_t mkh = (MODE == FP8KV_MODE_DENSE) ? 0u : Msk[8 + t / 4];
 #pragma unroll
       for (int k = 0; k < RPW; ++k) {
         const int i = warp * RPW + k;
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
         if (MODE == FP8KV_MODE_DENSE)
           vis = (n >= 0) && (tok < u1) && (tok < n);
         else
-          vis = (n >= 0) && (tok < u1) && ((mk >> (4 * n + (t & 3))) & 1u);
+          vis = (n >= 0) && (tok < u1) && sparse_bit(mk, mkh, n, t & 3);
         const float sv = vis ? fmaf(hi[k], c, lo[k] * c) : -INFINITY;
         float mt = sv;
 #pragma unroll

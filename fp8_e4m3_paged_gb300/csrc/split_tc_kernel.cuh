@@ -459,7 +459,7 @@ __device__ __noinline__ void patch_nonfinite_v(const Params& p, uint8_t* scratch
     const int tu = x / kC, c = x % kC;
     const uint8_t* row;
     int tok = 0, tk = 0;
-    uint32_t mk = 0u;
+    uint32_t mk = 0u, mkh = 0u;
     if (MODE == FP8KV_MODE_DENSE) {
       tok = u0 + tu;
       const int blk = p.block_table[(int64_t)b * p.bt_stride + tok / p.page_size];
@@ -469,8 +469,9 @@ __device__ __noinline__ void patch_nonfinite_v(const Params& p, uint8_t* scratch
       const int e = u0 + tu / 4;
       tk = tu % 4;
       mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
+      mkh = mask_hi_of(p.entry_mask_hi, p.entry_stride, b, e);
       const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-      if ((mk & (0x11111111u << tk)) == 0u || blk < 0 || blk >= p.num_kv_blocks) continue;
+      if (((mk | mkh) & (0x11111111u << tk)) == 0u || blk < 0 || blk >= p.num_kv_blocks) continue;
       row = p.v_cache + blk * p.vsb + tk * p.vst + g * p.vsh;
     }
     const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
@@ -485,7 +486,7 @@ __device__ __noinline__ void patch_nonfinite_v(const Params& p, uint8_t* scratch
       const int d = c * 16 + j;
       for (int i = 0; i < RC; ++i) {
         const int n = nrow[i];
-        const bool sees = (MODE == FP8KV_MODE_DENSE) ? (tok < n) : (n >= 0 && ((mk >> (4 * n + tk)) & 1u));
+        const bool sees = (MODE == FP8KV_MODE_DENSE) ? (tok < n) : (n >= 0 && sparse_bit(mk, mkh, n, tk));
         if (sees) atomicOr(&kinds[i * (D / 4) + d / 4], kind << (8 * (d % 4)));
       }
     }
@@ -682,7 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
       } else {
         const int e = u0 + i * kE + lane;
         const bool in = lane < kE && e < u1;
-        m = in ? p.entry_mask[(int64_t)b * p.entry_stride + e] : 0u;
+        // the copies only ask whether some row sees a token: both words folded
+        m = in ? (p.entry_mask[(int64_t)b * p.entry_stride + e] | mask_hi_of(p.entry_mask_hi, p.entry_stride, b, e))
+               : 0u;
         k = in ? p.entry_tbl[(int64_t)b * p.entry_stride + e] : 0;
       }
     };
@@ -1094,12 +1097,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
           const int e = u0 + i * kE + (r >> 2), tk = r & 3;
           if (e < u1) {
             uint32_t mk = p.entry_mask[(int64_t)b * p.entry_stride + e];
+            uint32_t mkh = mask_hi_of(p.entry_mask_hi, p.entry_stride, b, e);
             const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + e];
-            if (blk < 0 || blk >= p.num_kv_blocks) mk = 0u;
+            if (blk < 0 || blk >= p.num_kv_blocks) mk = mkh = 0u;
 #pragma unroll
             for (int n = 0; n < NL; ++n) {
               const int qr = mt.nrow[n];
-              vis |= ((qr >= 0) ? ((mk >> (4 * qr + tk)) & 1u) : 0u) << n;
+              vis |= ((qr >= 0) ? sparse_bit(mk, mkh, qr, tk) : 0u) << n;
             }
           }
         }
@@ -1288,17 +1292,18 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
 #pragma unroll
           for (int gq = 0; gq < 8; ++gq) {
             const int ent = u0 + i * kE + 2 * gq + ((lane & 3) >> 1);
-            uint32_t mk = 0u;
+            uint32_t mk = 0u, mkh = 0u;
             if (ent < u1) {
               mk = p.entry_mask[(int64_t)b * p.entry_stride + ent];
+              mkh = mask_hi_of(p.entry_mask_hi, p.entry_stride, b, ent);
               const int blk = p.entry_tbl[(int64_t)b * p.entry_stride + ent];
-              if (blk < 0 || blk >= p.num_kv_blocks) mk = 0u;
+              if (blk < 0 || blk >= p.num_kv_blocks) mk = mkh = 0u;
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int pos = (2 * (lane & 3) + e) & 3;
-              vis |= ((n_a >= 0) ? ((mk >> (4 * n_a + pos)) & 1u) : 0u) << (2 * gq + e);
-              vis |= ((n_b >= 0) ? ((mk >> (4 * n_b + pos)) & 1u) : 0u) << (16 + 2 * gq + e);
+              vis |= ((n_a >= 0) ? sparse_bit(mk, mkh, n_a, pos) : 0u) << (2 * gq + e);
+              vis |= ((n_b >= 0) ? sparse_bit(mk, mkh, n_b, pos) : 0u) << (16 + 2 * gq + e);
             }
           }
         }

@@ -31,7 +31,7 @@ class DeviceProblem:
         if p.mode == "dense":
             self.block_table = p.block_table.to(dev).contiguous()
             self.row_len = p.row_len.to(dev).contiguous()
-            self.entry_tbl = self.entry_mask = self.n_entries = None
+            self.entry_tbl = self.entry_mask = self.n_entries = self.entry_mask_hi = None
             mode = B.MODE_DENSE
             max_blocks = int(p.block_table.shape[1])
             max_kv_len = int(p.max_kv_len)
@@ -39,6 +39,8 @@ class DeviceProblem:
             self.block_table = self.row_len = None
             self.entry_tbl = p.entry_tbl.to(dev).contiguous()
             self.entry_mask = p.entry_mask.to(dev).contiguous()
+            hi = getattr(p, "entry_mask_hi", None)
+            self.entry_mask_hi = None if hi is None else hi.to(dev).contiguous()
             self.n_entries = p.n_entries.to(dev).contiguous()
             mode = B.MODE_SPARSE_PAGE4
             max_blocks = int(p.entry_tbl.shape[1])
@@ -65,6 +67,7 @@ class DeviceProblem:
             v_scale=0.0 if self.v_scale_dev is not None else p.v_scale,
             block_table=self.block_table, row_kv_len=self.row_len,
             entry_tbl=self.entry_tbl, entry_mask=self.entry_mask, n_entries=self.n_entries,
+            entry_mask_hi=self.entry_mask_hi,
             k_scale_dev=self.k_scale_dev, v_scale_dev=self.v_scale_dev)
         return B.Call(self.plan, args)
 

@@ -19,7 +19,8 @@
  *    with FP32 state", intro paragraphs 3 and 5.)
  *  - Sparse mode (QSA): four-token microblocks.  Entry e < n_entries[b] names
  *    physical microblock entry_tbl[b][e]; bit (4*r + t) of entry_mask[b][e]
- *    says that query row r sees token t of it.  Entries with mask 0 (the null
+ *    says that query row r < 8 sees token t of it, and bit (4*(r-8) + t) of
+ *    entry_mask_hi[b][e] the same for rows 8..15 (plans with q_max > 8).  Entries with mask 0 (the null
  *    padding entries) are never read, and unseen tokens contribute exactly
  *    zero whatever their bytes decode to, NaN included.  ("Qualify calibrated
  *    E4M3 and disk PLE with QSA DCP2", commit "grouped page4 null-block
@@ -69,7 +70,7 @@ extern "C" {
  * stale plan cannot reach kernels with another partial layout ("DFlash2 E4M3
  * attention with FP32 state", intro paragraph 5: the wrapper requires a given
  * precision capability revision). */
-#define FP8KV_ATTN_REVISION 4
+#define FP8KV_ATTN_REVISION 5
 
 /* Return codes. */
 #define FP8KV_OK 0
@@ -118,7 +119,7 @@ typedef struct CUstream_st* fp8kv_stream_t;
 typedef struct {
   int32_t mode;          /* FP8KV_MODE_* */
   int32_t batch;         /* B >= 0 requests (0: nothing to do) */
-  int32_t q_max;         /* query rows per request: 1..16 dense, 1..8 sparse */
+  int32_t q_max;         /* query rows per request: 1..16 (sparse above 8: args.entry_mask_hi) */
   int32_t num_q_heads;   /* Hq >= 1 */
   int32_t num_kv_heads;  /* Hkv >= 1, Hq % Hkv == 0 */
   int32_t head_dim;      /* D: 64, 128 or 256 */
@@ -184,6 +185,8 @@ typedef struct {
   void* out;                    /* fp16 [B][q_max][Hq][D], contiguous */
   void* workspace;              /* >= plan->workspace_bytes, 256-byte aligned */
   size_t workspace_bytes;
+  const uint32_t* entry_mask_hi; /* sparse with q_max > 8: [B][entry_stride] bits (4*(r-8) + t)
+                                    of rows 8..15 (required there; ignored with q_max <= 8) */
 } fp8kv_attn_args;
 
 /* Library revision (FP8KV_ATTN_REVISION). */
@@ -310,7 +313,8 @@ int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, fp8kv_stream
  * m = t / 4 that any query row selected (positions t >= 0, below
  * 4 * max_blocks), in increasing order, become entries with
  *   entry_tbl[b][e]  = block_table[b][m]          (physical microblock)
- *   entry_mask[b][e] = OR over selections t of row r in m of bit 4r + t%4
+ *   entry_mask[b][e] = OR over selections t of row r < 8 in m of bit 4r + t%4
+ *   entry_mask_hi[b][e] = the same for rows 8..15 (bit 4(r-8) + t%4; q_max > 8)
  * and null entries (null_block, mask 0) pad the count to a multiple of 8;
  * n_entries[b] is the padded count ("Qualify calibrated E4M3 and disk PLE
  * with QSA DCP2", commit "grouped page4 null-block padding").  Duplicate
@@ -321,7 +325,7 @@ int fp8kv_attn_merge_scale(const fp8kv_merge_args* a, int32_t rank, fp8kv_stream
  * ------------------------------------------------------------------------ */
 typedef struct {
   int32_t batch;                /* B >= 0 */
-  int32_t q_max;                /* query rows per request, 1..8 (32-bit masks) */
+  int32_t q_max;                /* query rows per request, 1..16 (above 8: entry_mask_hi) */
   int32_t topk;                 /* selection slots per row, >= 0 */
   int32_t max_blocks;           /* logical microblocks per request, >= 1 */
   int32_t null_block;           /* physical microblock of padding entries */
@@ -333,6 +337,7 @@ typedef struct {
   int64_t entry_stride;         /* elements, >= q_max * topk rounded up to 8 */
   int32_t* n_entries;           /* [B] */
   uint32_t* status;             /* optional status word, NULL = none */
+  uint32_t* entry_mask_hi;      /* q_max > 8: [B][entry_stride] bits 4*(r-8) + t%4 of rows 8..15 */
 } fp8kv_select_args;
 
 int fp8kv_attn_select_to_entries(const fp8kv_select_args* a, fp8kv_stream_t stream);

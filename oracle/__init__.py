@@ -93,6 +93,7 @@ class OrcProblem(ctypes.Structure):
         ("n_entries", ctypes.c_void_p), ("entry_stride", ctypes.c_int64),
         ("softmax_scale", ctypes.c_double), ("k_scale", ctypes.c_double),
         ("v_scale", ctypes.c_double), ("kv_format", ctypes.c_int),
+        ("entry_mask_hi", ctypes.c_void_p),
     ]
 
 
@@ -180,6 +181,11 @@ class _Pinned:
             s.entry_mask = em.data_ptr()
             s.n_entries = ne.data_ptr()
             s.entry_stride = et.shape[1]
+            hi = getattr(p, "entry_mask_hi", None)
+            if hi is not None:
+                hi = hi.contiguous()
+                self.keep.append(hi)
+                s.entry_mask_hi = hi.data_ptr()
         s.softmax_scale = p.softmax_scale
         s.k_scale = p.k_scale
         s.v_scale = p.v_scale
@@ -327,7 +333,8 @@ def merge(outs, lses, plant: int = 0):
     return m, lm
 
 
-def select_to_entries(sel, block_table, max_blocks: int, null_block: int, entry_stride: Optional[int] = None):
+def select_to_entries(sel, block_table, max_blocks: int, null_block: int, entry_stride: Optional[int] = None,
+                      with_hi: bool = False):
     """The grouped planner, from its definition ("Qualify calibrated E4M3 and
     disk PLE with QSA DCP2", commit "grouped page4 null-block padding").
 
@@ -335,10 +342,12 @@ def select_to_entries(sel, block_table, max_blocks: int, null_block: int, entry_
     unused; positions at or past 4 * max_blocks are ignored and counted).
     For each request: the distinct four-token logical microblocks m = t // 4
     any row selected, in increasing order; entry_tbl = block_table[b][m];
-    bit 4r + t % 4 of entry_mask set iff row r selected token t; then null
+    bit 4r + t % 4 of entry_mask set iff row r < 8 selected token t (rows
+    8..15: bit 4(r - 8) + t % 4 of the second word entry_mask_hi); then null
     entries (null_block, mask 0) up to a multiple of 8.
     Returns (entry_tbl [B][stride] int32, entry_mask [B][stride] uint32,
-    n_entries [B] int32, n_ignored)."""
+    n_entries [B] int32, n_ignored), and entry_mask_hi [B][stride] uint32
+    after them when with_hi."""
     sel = np.asarray(sel, dtype=np.int64)
     bt = np.asarray(block_table, dtype=np.int64)
     B, q, _ = sel.shape
@@ -364,11 +373,16 @@ def select_to_entries(sel, block_table, max_blocks: int, null_block: int, entry_
     stride = entry_stride or max(8, max(len(e) for e in per_req))
     tbl = np.zeros((B, stride), dtype=np.int32)
     msk = np.zeros((B, stride), dtype=np.uint32)
+    msk_hi = np.zeros((B, stride), dtype=np.uint32)
     n = np.zeros(B, dtype=np.int32)
     for b, ent in enumerate(per_req):
         assert len(ent) <= stride, "entries exceed the stride"
         n[b] = len(ent)
         for e, (t, m) in enumerate(ent):
             tbl[b, e] = t
-            msk[b, e] = m
+            msk[b, e] = m & 0xFFFFFFFF
+            msk_hi[b, e] = m >> 32
+    if with_hi:
+        return tbl, msk, n, ignored, msk_hi
+    assert q <= 8 or not msk_hi.any(), "rows 8..15 need with_hi"
     return tbl, msk, n, ignored

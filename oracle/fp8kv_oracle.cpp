@@ -69,6 +69,7 @@ typedef struct {
   int64_t entry_stride;
   double softmax_scale, k_scale, v_scale;
   int kv_format;  // cache byte format: 0 = E4M3 (E4M3FN), 1 = E5M2
+  const uint32_t* entry_mask_hi; // sparse rows 8..15: [B][entry_stride], NULL for q <= 8
 } orc_problem;
 
 // ORC_PLANT (compile-time, default 0 = none) plants one plausible mistake;
@@ -250,12 +251,15 @@ static void visible(const orc_problem* p, int b, int r, int g, std::vector<Tok>&
     const int ne = p->n_entries[b];
     for (int e = 0; e < ne; ++e) {
       const int64_t blk = p->entry_tbl[(int64_t)b * p->entry_stride + e];
-      const uint32_t msk = p->entry_mask[(int64_t)b * p->entry_stride + e];
+      // rows 0..7: bit 4r + t of the first word; rows 8..15: bit 4(r - 8) + t
+      // of the second
+      const uint32_t msk = r < 8 ? p->entry_mask[(int64_t)b * p->entry_stride + e]
+                                 : p->entry_mask_hi[(int64_t)b * p->entry_stride + e];
         for (int t = 0; t < 4; ++t) {
 #if ORC_PLANT == 6
-        if ((msk >> (8 * t + r)) & 1u) {  // planted: transposed mask bit layout
+        if ((msk >> (8 * t + (r & 7))) & 1u) {  // planted: transposed mask bit layout
 #else
-        if ((msk >> (4 * r + t)) & 1u) {
+        if ((msk >> (4 * (r & 7) + t)) & 1u) {
 #endif
           out.push_back({blk * p->k_stride[0] + (int64_t)t * p->k_stride[1] + (int64_t)g * p->k_stride[2],
                          blk * p->v_stride[0] + (int64_t)t * p->v_stride[1] + (int64_t)g * p->v_stride[2]});
@@ -449,7 +453,7 @@ static void row_head_split(const orc_problem* p, int b, int r, int h, int S_, do
 static int check(const orc_problem* p) {
   if (!p || p->B < 0 || p->q < 1 || p->Hq < 1 || p->Hkv < 1 || p->D < 1) return -1;
   if (p->Hq % p->Hkv) return -1;
-  if (p->mode == 1 && p->q > 8) return -1;
+  if (p->mode == 1 && (p->q > 16 || (p->q > 8 && !p->entry_mask_hi))) return -1;
   if (p->kv_format != 0 && p->kv_format != 1) return -1;
   return 0;
 }

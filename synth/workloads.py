@@ -63,7 +63,8 @@ class Problem:
       block_table  [B][max_pages]           torch.int32   (dense)
       row_len      [B][q]                   torch.int32   (dense; 0 = dead row)
       entry_tbl    [B][max_entries]         torch.int32   (sparse)
-      entry_mask   [B][max_entries]         torch.int32   (sparse; uint32 bits)
+      entry_mask   [B][max_entries]         torch.int32   (sparse; uint32 bits, rows 0..7)
+      entry_mask_hi[B][max_entries]         torch.int32   (sparse, q > 8; rows 8..15)
       n_entries    [B]                      torch.int32   (sparse)
     """
 
@@ -89,6 +90,7 @@ class Problem:
     n_entries: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
     kv_format: str = "e4m3"       # cache byte format: "e4m3" (E4M3FN) or "e5m2"
+    entry_mask_hi: Optional[torch.Tensor] = None  # sparse rows 8..15 (q > 8)
 
     @property
     def num_blocks(self) -> int:
@@ -306,9 +308,10 @@ def make_sparse(
     """Build a QSA sparse problem over 4-token microblocks.
 
     Mask bit (4*r + t) set <=> query row r sees token t of that entry's
-    microblock.  Padding entries are (microblock 0, mask 0).
+    microblock: rows 0..7 in entry_mask, rows 8..15 (bit 4*(r-8) + t) in
+    entry_mask_hi (q > 8 only).  Padding entries are (microblock 0, mask 0).
     """
-    assert q <= 8, "32-bit masks hold 8 rows of 4 tokens"
+    assert q <= 16, "two 32-bit mask words hold 16 rows of 4 tokens"
     P = 4
     nmb = math.ceil(L / P)
     total = B * nmb
@@ -365,13 +368,16 @@ def make_sparse(
     max_e = max(max_e, pad_to)
     entry_tbl = torch.zeros((B, max_e), dtype=torch.int32)
     entry_mask = torch.zeros((B, max_e), dtype=torch.int64)
+    entry_mask_hi = torch.zeros((B, max_e), dtype=torch.int64)
     n_entries = torch.zeros((B,), dtype=torch.int32)
     for b in range(B):
         n = len(tbls[b])
         entry_tbl[b, :n] = torch.tensor(tbls[b], dtype=torch.int32)
-        entry_mask[b, :n] = torch.tensor(masks[b], dtype=torch.int64)
+        entry_mask[b, :n] = torch.tensor([m & 0xFFFFFFFF for m in masks[b]], dtype=torch.int64)
+        entry_mask_hi[b, :n] = torch.tensor([m >> 32 for m in masks[b]], dtype=torch.int64)
         n_entries[b] = n
     entry_mask = _u32_bits(entry_mask)
+    entry_mask_hi = _u32_bits(entry_mask_hi) if q > 8 else None
 
     q16 = _gauss(_seed(seed, 14), (B, q, Hq, D), False).to(torch.float16)
     return Problem(
@@ -379,7 +385,7 @@ def make_sparse(
         q_fp16=q16, k_cache=k_cache, v_cache=v_cache,
         softmax_scale=_f32(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D)),
         k_scale=float(ks), v_scale=float(vs), max_kv_len=L,
-        entry_tbl=entry_tbl, entry_mask=entry_mask, n_entries=n_entries,
+        entry_tbl=entry_tbl, entry_mask=entry_mask, n_entries=n_entries, entry_mask_hi=entry_mask_hi,
         meta={"L": L, "topk_blocks": topk_blocks, "seed": seed,
               # logical microblock -> physical microblock of every request
               "block_table": phys_of.to(torch.int32)},
@@ -395,8 +401,25 @@ def _u32_bits(x64: torch.Tensor) -> torch.Tensor:
 
 
 def masks_u32(p: Problem) -> torch.Tensor:
-    """The sparse masks as non-negative int64 values (for host-side logic)."""
+    """The sparse masks of rows 0..7 as non-negative int64 values (host-side logic)."""
     return p.entry_mask.to(torch.int64) & 0xFFFFFFFF
+
+
+def masks_u64(p: Problem) -> torch.Tensor:
+    """All 16 rows' sparse bits as int64 values: bit 4r + t for r < 16 (the
+    second word shifted up by 32; bit 63 may make the value negative)."""
+    lo = p.entry_mask.to(torch.int64) & 0xFFFFFFFF
+    if p.entry_mask_hi is None:
+        return lo
+    return lo | (p.entry_mask_hi.to(torch.int64) << 32)
+
+
+def masks_any(p: Problem) -> torch.Tensor:
+    """Per entry, bit 4k + t set iff some row sees token t (both words folded)."""
+    m = masks_u32(p)
+    if p.entry_mask_hi is not None:
+        m = m | (p.entry_mask_hi.to(torch.int64) & 0xFFFFFFFF)
+    return m
 
 
 # --------------------------------------------------------------------------
@@ -450,7 +473,7 @@ def attended_kv_bytes(p: Problem) -> int:
             u = int(p.row_len[b].max()) if p.q > 0 else 0
             tot += u
         return tot * p.Hkv * 2 * p.D
-    m = masks_u32(p)
+    m = masks_any(p)
     tot = 0
     for b in range(p.B):
         n = int(p.n_entries[b])

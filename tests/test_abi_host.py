@@ -84,7 +84,7 @@ def test_plan_split_override_and_batch0(B):
     (dict(num_kv_blocks=0), -1),
     (dict(mode=7), -1),
     (dict(mode=1, page_size=16), -2),
-    (dict(mode=1, page_size=4, q_max=9), -2),
+    (dict(mode=1, page_size=4, q_max=17), -2),
     (dict(batch=-1), -1),
     (dict(num_splits=-3), -1),
 ])
@@ -125,6 +125,17 @@ def test_launch_validation(B, kw, code):
     a = _fake_args(B, plan, **kw)
     for fn in (B.lib.fp8kv_attn_split, B.lib.fp8kv_attn_combine):
         assert fn(ctypes.byref(plan), ctypes.byref(a), None) == code
+
+
+def test_sparse_rows_past_8_need_the_second_mask_words(B):
+    """A sparse plan with 9..16 query rows is accepted; its launch needs
+    entry_mask_hi (rows 8..15), checked on the host before any CUDA call."""
+    plan = B.fp8kv_attn_plan(_desc(B, mode=1, page_size=4, q_max=12, max_kv_len=0, max_blocks=64))
+    assert plan.q_max == 12 and plan.rows == 12 * plan.group
+    fake = 1 << 20
+    a = _fake_args(B, plan, block_table=None, row_kv_len=None, entry_tbl=fake, entry_mask=fake,
+                   n_entries=fake, entry_stride=64)
+    assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == B.EINVAL
 
 
 def test_launch_workspace_and_revision(B):
@@ -193,7 +204,7 @@ def _sel(B, **kw):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(batch=-1), dict(q_max=0), dict(q_max=9), dict(topk=-1), dict(max_blocks=0),
+    dict(batch=-1), dict(q_max=0), dict(q_max=9), dict(q_max=17), dict(topk=-1), dict(max_blocks=0),
     dict(block_table_stride=99), dict(entry_stride=63), dict(sel=0), dict(block_table=0), dict(entry_tbl=0),
     dict(entry_mask=0), dict(n_entries=0),
 ])

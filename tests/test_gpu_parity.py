@@ -189,6 +189,27 @@ def test_shapes_sparse(D, q, Hq, Hkv):
     compare(got, oracle.attention(p), what=f"sparse D={D} q={q}")
 
 
+@pytest.mark.parametrize("q,Hq,Hkv,D,kernel", [
+    (12, 24, 2, 128, 0),   # 144 rows: three row chunks on the query-row tensor-core kernel
+    (12, 24, 2, 128, 1),   # the CUDA-core kernel
+    (16, 2, 2, 128, 0),    # 16 rows: the small-group tensor-core kernel
+    (9, 2, 2, 256, 3),     # 9 rows, D = 256, small group
+    (16, 32, 2, 128, 2),   # 256 rows: four row chunks
+    (16, 16, 4, 64, 1),    # D = 64: CUDA-core only
+])
+def test_sparse_rows_past_8(q, Hq, Hkv, D, kernel):
+    """Sparse verify with 9..16 query rows: rows 8..15 read the second mask
+    word.  Every row sees a different causal prefix of its own top-k."""
+    p = make_sparse(B=2, q=q, Hq=Hq, Hkv=Hkv, D=D, L=12000, topk_blocks=200, seed=500 + q * 7 + D)
+    assert p.entry_mask_hi is not None and int(p.entry_mask_hi.abs().sum()) > 0
+    dp = _dp(p, kernel=kernel)
+    if kernel:
+        assert dp.plan.kernel == kernel
+    got = _run(dp)
+    compare(got, oracle.attention(p), what=f"sparse q={q} Hq={Hq} D={D} kernel {dp.plan.kernel}")
+    assert dp.status() == 0
+
+
 def test_device_scales():
     p = _problem("c2")
     got = _run(_dp(p, device_scales=True))

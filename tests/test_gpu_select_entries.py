@@ -40,35 +40,44 @@ def _gpu_plan(sel, bt, max_blocks, null_block):
     dev = torch.device("cuda")
     tbl = torch.full((Bn, stride), -7, dtype=torch.int32, device=dev)
     msk = torch.full((Bn, stride), -7, dtype=torch.int32, device=dev)
+    msk_hi = torch.full((Bn, stride), -7, dtype=torch.int32, device=dev) if q > 8 else None
     n = torch.zeros(Bn, dtype=torch.int32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     a = B.make_select_args(sel=torch.as_tensor(sel, dtype=torch.int32).to(dev).contiguous(),
                            block_table=torch.as_tensor(bt, dtype=torch.int32).to(dev).contiguous(),
                            max_blocks=max_blocks, null_block=null_block, entry_tbl=tbl, entry_mask=msk,
-                           n_entries=n, status=st)
+                           n_entries=n, status=st, entry_mask_hi=msk_hi)
     B.fp8kv_attn_select_to_entries(a, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
-    return tbl.cpu().numpy(), msk.cpu().numpy().view(np.uint32), n.cpu().numpy(), int(st.item())
+    out = (tbl.cpu().numpy(), msk.cpu().numpy().view(np.uint32), n.cpu().numpy(), int(st.item()))
+    if q > 8:
+        out = out + (msk_hi.cpu().numpy().view(np.uint32),)
+    return out
 
 
 def _same(got, ref):
-    tbl, msk, n, _ = got
-    rt, rm, rn, _ = ref
+    tbl, msk, n = got[:3]
+    rt, rm, rn = ref[:3]
     assert np.array_equal(n, rn)
     for b in range(len(n)):
         assert np.array_equal(tbl[b, :n[b]], rt[b, :n[b]]), b
         assert np.array_equal(msk[b, :n[b]], rm[b, :n[b]]), b
+        if len(got) > 4:  # rows 8..15
+            assert np.array_equal(got[4][b, :n[b]], ref[4][b, :n[b]]), b
         assert bool((tbl[b, n[b]:] == -7).all())  # nothing written past the count
 
 
-@pytest.mark.parametrize("q,topk,L", [(1, 100, 500), (2, 512, 8192), (4, 1000, 50000), (8, 2048, 131072)])
+@pytest.mark.parametrize("q,topk,L", [(1, 100, 500), (2, 512, 8192), (4, 1000, 50000), (8, 2048, 131072),
+                                     (12, 1024, 131072), (16, 512, 70000)])
 def test_planner_matches_oracle(q, topk, L):
+    """Rows 9..16 use two mask words and chunks of 16384 microblocks (the
+    131072-token and 70000-token contexts span two and two chunks)."""
     p = make_sparse(name="pl", B=3, q=q, Hq=q, Hkv=1, D=64, L=L, topk_blocks=2, seed=q)
     bt = p.meta["block_table"].numpy()
     sel = make_selection(3, q, L, topk, seed=11 + q, past_end=2).numpy()
     got = _gpu_plan(sel, bt, bt.shape[1], 0)
-    ref = orc_ref = oracle.select_to_entries(sel, bt, bt.shape[1], 0)
-    _same(got, orc_ref)
+    ref = oracle.select_to_entries(sel, bt, bt.shape[1], 0, with_hi=True)
+    _same(got, ref if q > 8 else ref[:4])
     assert got[3] == 4 and ref[3] == 2  # FP8KV_STATUS_BAD_ENTRIES; two positions ignored
 
 
@@ -110,4 +119,32 @@ def test_planner_feeds_sparse_attention():
     p3 = dataclasses.replace(p, entry_tbl=torch.from_numpy(rt), entry_mask=torch.from_numpy(rm.view(np.int32)),
                              n_entries=torch.from_numpy(rn))
     compare(out.float().cpu().numpy(), oracle.attention(p3), what="planner -> sparse attention")
+    assert dp.status() == 0
+
+
+def test_planner_feeds_sparse_attention_12_rows():
+    """12 query rows (masks in two words) from selections to attention."""
+    from fp8_e4m3_paged_gb300.device_problem import DeviceProblem
+
+    q, L, topk = 12, 32768, 512
+    p = make_sparse(name="pl", B=2, q=q, Hq=24, Hkv=2, D=128, L=L, topk_blocks=2, seed=19)
+    bt = p.meta["block_table"].numpy()
+    sel = make_selection(2, q, L, topk, seed=6).numpy()
+    tbl, msk, n, st, msk_hi = _gpu_plan(sel, bt, bt.shape[1], 0)
+    assert st == 0
+    stride = tbl.shape[1]
+    live = np.arange(stride)[None, :] < n[:, None]
+    tbl = np.where(live, tbl, 0).astype(np.int32)
+    msk = np.where(live, msk, 0).astype(np.uint32)
+    msk_hi = np.where(live, msk_hi, 0).astype(np.uint32)
+    p2 = dataclasses.replace(p, entry_tbl=torch.from_numpy(tbl), entry_mask=torch.from_numpy(msk.view(np.int32)),
+                             entry_mask_hi=torch.from_numpy(msk_hi.view(np.int32)),
+                             n_entries=torch.from_numpy(n.astype(np.int32)))
+    dp = DeviceProblem(p2)
+    out = dp.run()
+    torch.cuda.synchronize()
+    rt, rm, rn, _, rh = oracle.select_to_entries(sel, bt, bt.shape[1], 0, entry_stride=stride, with_hi=True)
+    p3 = dataclasses.replace(p, entry_tbl=torch.from_numpy(rt), entry_mask=torch.from_numpy(rm.view(np.int32)),
+                             entry_mask_hi=torch.from_numpy(rh.view(np.int32)), n_entries=torch.from_numpy(rn))
+    compare(out.float().cpu().numpy(), oracle.attention(p3), what="planner -> sparse attention, 12 rows")
     assert dp.status() == 0

@@ -113,7 +113,8 @@ def _pins():
         cf.test_scale_roles,
         cf.test_weights_sum_to_one,
         iv.test_gqa_grouping,
-        iv.test_sparse_all_visible_equals_dense,
+        lambda o: iv.test_sparse_all_visible_equals_dense(o, 3),
+        lambda o: iv.test_sparse_all_visible_equals_dense(o, 12),
         test_qsa_mask_rule,
         lambda o: bf.test_dense_tiny_exact(o, 1),
         lambda o: bf.test_sparse_tiny_exact(o, 6),

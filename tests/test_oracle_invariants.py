@@ -10,6 +10,7 @@
 """
 
 import numpy as np
+import pytest
 import torch
 
 from synth import make_dense, make_sparse
@@ -71,8 +72,10 @@ def test_sparse_order_and_padding(orc):
     assert np.array_equal(c, b_)
 
 
-def test_sparse_all_visible_equals_dense(orc):
-    L, q = 61, 3
+@pytest.mark.parametrize("q", [3, 12, 16])
+def test_sparse_all_visible_equals_dense(orc, q):
+    """Rows 8..15 (q > 8) take their bits from the second mask word."""
+    L = 61
     d = make_dense(B=1, q=q, Hq=2, Hkv=1, D=16, page_size=4, lens=[L], seed=24)
     # same physical pool viewed as microblocks, every causal token visible
     nmb = (L + 3) // 4
@@ -85,11 +88,13 @@ def test_sparse_all_visible_equals_dense(orc):
                 if 4 * m + t < n_r:
                     bits |= 1 << (4 * r + t)
         masks.append(bits)
-    s = make_sparse(B=1, q=q, Hq=2, Hkv=1, D=16, L=8, topk_blocks=1, seed=0)
+    s = make_sparse(B=1, q=q, Hq=2, Hkv=1, D=16, L=max(8, q), topk_blocks=1, seed=0)
     s.k_cache, s.v_cache, s.q_fp16 = d.k_cache, d.v_cache, d.q_fp16
     s.softmax_scale, s.k_scale, s.v_scale = d.softmax_scale, d.k_scale, d.v_scale
     s.entry_tbl = d.block_table[:, :nmb].clone()
-    s.entry_mask = _u32_bits(torch.tensor([masks], dtype=torch.int64))
+    s.entry_mask = _u32_bits(torch.tensor([[m & 0xFFFFFFFF for m in masks]], dtype=torch.int64))
+    s.entry_mask_hi = _u32_bits(torch.tensor([[m >> 32 for m in masks]], dtype=torch.int64)) if q > 8 else None
+    s.q = q
     s.n_entries = torch.tensor([nmb], dtype=torch.int32)
     assert np.array_equal(orc.attention(s), orc.attention(d))
     assert int(masks_u32(s).max()) < 2**32

@@ -32,8 +32,12 @@ def test_hand_worked_case(orc):
     assert n.tolist() == g["n_entries"] and ign == 0
 
 
-def _check_invariants(sel, bt, max_blocks, null, tbl, msk, n):
+def _check_invariants(sel, bt, max_blocks, null, tbl, msk, n, msk_hi=None):
+    """msk_hi (rows 8..15) joins msk as the upper 32 bits of one 64-bit mask."""
     B, q, _ = sel.shape
+    msk = msk.astype(np.uint64)
+    if msk_hi is not None:
+        msk = msk | (msk_hi.astype(np.uint64) << np.uint64(32))
     for b in range(B):
         ne = int(n[b])
         assert ne % 8 == 0
@@ -57,15 +61,17 @@ def _check_invariants(sel, bt, max_blocks, null, tbl, msk, n):
         assert len(phys) == len(real)
 
 
-@pytest.mark.parametrize("q,topk,L", [(1, 64, 300), (4, 48, 1000), (8, 200, 4000)])
+@pytest.mark.parametrize("q,topk,L", [(1, 64, 300), (4, 48, 1000), (8, 200, 4000), (12, 64, 2000),
+                                     (16, 32, 1000)])
 def test_invariants(orc, q, topk, L):
     p = make_sparse(name="pl", B=3, q=q, Hq=2 * q if q <= 4 else q, Hkv=1, D=64, L=L, topk_blocks=4, seed=q)
     bt = p.meta["block_table"].numpy()
     sel = make_selection(3, q, L, topk, seed=7 + q, past_end=3).numpy()
     mb = bt.shape[1]
-    tbl, msk, n, ign = orc.select_to_entries(sel, bt, mb, 0)
+    tbl, msk, n, ign, msk_hi = orc.select_to_entries(sel, bt, mb, 0, with_hi=True)
     assert ign == 3
-    _check_invariants(sel, bt, mb, 0, tbl, msk, n)
+    assert (q > 8) == bool(msk_hi.any())
+    _check_invariants(sel, bt, mb, 0, tbl, msk, n, msk_hi)
 
 
 def test_empty_selection_gives_no_entries(orc):
