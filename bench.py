@@ -277,6 +277,7 @@ def run_ours(args):
         "config": {
             "workload": f"{args.workload}: {WORKLOAD_DESC.get(args.workload, '')}",
             "attended_kv_bytes_per_step": bytes_step,
+            "kv_format": args.kv_format,
             "kernel": {1: "generic (CUDA cores)", 2: "tcgen05 (query rows)",
                        3: "tcgen05 small group (tokens as rows)"}.get(dp.plan.kernel, str(dp.plan.kernel)),
             "num_splits": dp.plan.num_splits,
@@ -457,11 +458,14 @@ def cpu_baseline(p, bytes_step, budget_s=15.0):
 def _overrides(args):
     """--reqs N: the first N requests of the batched decode workload (same
     lengths and bytes as the full batch's first N), for small profiles."""
+    over = {}
     if args.reqs:
         if args.workload != "c4":
             raise SystemExit("--reqs applies to the batched decode workload (c4) only")
-        return {"B": args.reqs}
-    return {}
+        over["B"] = args.reqs
+    if args.kv_format != "e4m3":
+        over["kv_format"] = args.kv_format
+    return over
 
 
 def run_reference(args):
@@ -477,7 +481,7 @@ def run_reference(args):
 
     oracle.build()
     threads = oracle.default_threads()
-    p = make_problem(args.workload)
+    p = make_problem(args.workload, **_overrides(args))
     bytes_step = attended_kv_bytes(p)
     allitems = [(b, r, h) for b in range(p.B) for r in range(p.q) for h in range(p.Hq)]
     # cost of one query vector
@@ -907,6 +911,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reqs", type=int, default=0, help="c4 only: the first N of its 64 requests")
+    ap.add_argument("--kv-format", choices=["e4m3", "e5m2", "bf16"], default="e4m3",
+                    help="cache format (bf16: the unquantised cache, for A/B against the FP8 path)")
     ap.add_argument("--op", choices=["attention", "cache_write", "dcp_merge", "select_entries"], default="attention")
     args = ap.parse_args()
     if args.warmup < 3:

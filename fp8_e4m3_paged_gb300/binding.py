@@ -28,6 +28,7 @@ MODE_SPARSE_PAGE4 = 1
 
 KV_E4M3 = 0
 KV_E5M2 = 1
+KV_BF16 = 2
 
 KERNEL_AUTO = 0
 KERNEL_GENERIC = 1

@@ -49,7 +49,11 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   if ((d->kernel == FP8KV_KERNEL_TC || d->kernel == FP8KV_KERNEL_TC_SMALL) && d->head_dim != 128 &&
       d->head_dim != 256)
     return FP8KV_EUNSUPPORTED;
-  if (d->kv_format != FP8KV_KV_E4M3 && d->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
+  if (d->kv_format != FP8KV_KV_E4M3 && d->kv_format != FP8KV_KV_E5M2 && d->kv_format != FP8KV_KV_BF16)
+    return FP8KV_EINVAL;
+  // bf16 caches: the CUDA-core kernel only
+  if (d->kv_format == FP8KV_KV_BF16 && d->kernel != FP8KV_KERNEL_AUTO && d->kernel != FP8KV_KERNEL_GENERIC)
+    return FP8KV_EUNSUPPORTED;
   if (d->test_flags & ~FP8KV_TEST_STALL_PIPELINE) return FP8KV_EINVAL;
   if (d->mode == FP8KV_MODE_DENSE) {
     if ((int64_t)d->max_blocks * d->page_size < d->max_kv_len) return FP8KV_EINVAL;
@@ -94,7 +98,9 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   const bool tc_dims = P.head_dim == 128 || P.head_dim == 256;
   int kind = d->kernel;
   if (kind == FP8KV_KERNEL_AUTO)
-    kind = !tc_dims ? FP8KV_KERNEL_GENERIC : (P.rows <= kTcSmallRows ? FP8KV_KERNEL_TC_SMALL : FP8KV_KERNEL_TC);
+    kind = (!tc_dims || d->kv_format == FP8KV_KV_BF16)
+               ? FP8KV_KERNEL_GENERIC
+               : (P.rows <= kTcSmallRows ? FP8KV_KERNEL_TC_SMALL : FP8KV_KERNEL_TC);
   int tile, ctas_per_sm, max_part_tiles;
   if (kind == FP8KV_KERNEL_TC || kind == FP8KV_KERNEL_TC_SMALL) {
     const bool small = kind == FP8KV_KERNEL_TC_SMALL;
@@ -179,7 +185,9 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->kv_format = plan->kv_format;
   p->test_flags = plan->test_flags;
   p->min_part = plan->min_part;
-  if (p->kv_format != FP8KV_KV_E4M3 && p->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
+  if (p->kv_format != FP8KV_KV_E4M3 && p->kv_format != FP8KV_KV_E5M2 && p->kv_format != FP8KV_KV_BF16)
+    return FP8KV_EINVAL;
+  if (p->kv_format == FP8KV_KV_BF16 && plan->kernel != kGeneric) return FP8KV_EINVAL;
   if (p->G < 1 || p->rows != p->q_max * p->G || p->S < 1 || p->row_chunk < 1) return FP8KV_EINVAL;
 
   if (!a->workspace || !aligned(a->workspace, 256)) return FP8KV_EINVAL;

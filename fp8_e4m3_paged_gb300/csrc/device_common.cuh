@@ -64,6 +64,14 @@ __device__ __forceinline__ uint32_t nonfinite_codes(const uint4& w, bool e5m2) {
   return (((w.x & m) + a) | ((w.y & m) + a) | ((w.z & m) + a) | ((w.w & m) + a)) & 0x80808080u;
 }
 
+// Nonzero iff one of the eight bf16 values in w is an infinity or a NaN
+// (exponent bits all ones): per 16-bit half, (h & 0x7F80) + 0x80 reaches bit
+// 15 only from 0x7F80, and no carry crosses the halves.
+__device__ __forceinline__ uint32_t nonfinite_bf16(const uint4& w) {
+  const uint32_t m = 0x7F807F80u, a = 0x00800080u;
+  return (((w.x & m) + a) | ((w.y & m) + a) | ((w.z & m) + a) | ((w.w & m) + a)) & 0x80008000u;
+}
+
 // The four bytes of x with every non-finite code replaced by 0.
 __device__ __forceinline__ uint32_t zap_nonfinite(uint32_t x, bool e5m2) {
   const uint32_t m = e5m2 ? 0x7C7C7C7Cu : 0x7F7F7F7Fu;

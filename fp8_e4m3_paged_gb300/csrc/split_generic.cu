@@ -2,9 +2,9 @@
 //
 // One CTA handles one (partition s, KV head g, row chunk, request b).  It
 // keeps up to 64 query vectors (query rows x heads of the group) in shared
-// memory, streams its token range of the E4M3 pages in tiles of 32 tokens
-// (dense) or 8 four-token microblocks (sparse) with 16-byte loads, decodes the
-// bytes exactly to FP32, and runs the online softmax with FP32 state:
+// memory, streams its token range of the cache pages (E4M3 or E5M2 bytes, or
+// bf16 values for A/B runs) in tiles of 32 tokens (dense) or 8 four-token
+// microblocks (sparse) with 16-byte loads, decodes them exactly to FP32, and runs the online softmax with FP32 state:
 //   s = (q . k) * softmax_scale * k_scale * log2(e)
 //   m' = max(m, ceil(max_tile s));  acc = acc * 2^(m - m') + sum_t 2^(s_t - m') v_t
 //   l  = l * 2^(m - m') + sum_t 2^(s_t - m')
@@ -17,6 +17,7 @@
 // infinity) code in V skips the tokens each row does not see, so the code
 // reaches exactly the rows that see its token, as in the exact softmax.
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda_runtime.h>
 
@@ -161,8 +162,7 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
   for (int tb = u0; tb < u1; tb += unit) {
     bool vbad = false;  // this thread loaded a non-finite V code
     // ------------------------------------------------------ load + decode
-    // 16-byte vectors: TT tokens x D/16 vectors for K and for V.
-    constexpr int VPT = D / 16;
+    // 16-byte vectors: TT tokens x D/16 (FP8) or D/8 (bf16) vectors for K and for V.
     if (MODE == FP8KV_MODE_SPARSE_PAGE4 && tid < 8) {
       const int e = tb + tid;
       uint32_t mk = 0, mkh = 0;
@@ -179,8 +179,11 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
       Msk[8 + tid] = mkh;
     }
     if (MODE == FP8KV_MODE_SPARSE_PAGE4) __syncthreads();
-    for (int idx = tid; idx < TT * VPT; idx += NT) {
-      const int t = idx / VPT, vv = idx % VPT;
+    // VPTL 16-byte vectors per token row: D/16 of FP8 bytes, D/8 of bf16
+    auto load_tile = [&](auto vpt_c) {
+    constexpr int VPTL = decltype(vpt_c)::value;
+    for (int idx = tid; idx < TT * VPTL; idx += NT) {
+      const int t = idx / VPTL, vv = idx % VPTL;
       bool ok = false;
       const uint8_t* kp = nullptr;
       const uint8_t* vp = nullptr;
@@ -213,6 +216,19 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
         kw = __ldg(reinterpret_cast<const uint4*>(kp) + vv);
         vw = __ldg(reinterpret_cast<const uint4*>(vp) + vv);
       }
+      if constexpr (VPTL == D / 8) {
+        // bf16: the upper half of an FP32 word, exact
+        vbad |= nonfinite_bf16(vw) != 0u;
+        const uint32_t kwa[4] = {kw.x, kw.y, kw.z, kw.w};
+        const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          Ks[t * (D + 1) + vv * 8 + j * 2] = __uint_as_float(kwa[j] << 16);
+          Ks[t * (D + 1) + vv * 8 + j * 2 + 1] = __uint_as_float(kwa[j] & 0xFFFF0000u);
+          *reinterpret_cast<float2*>(&Vs[t * D + vv * 8 + j * 2]) =
+              make_float2(__uint_as_float(vwa[j] << 16), __uint_as_float(vwa[j] & 0xFFFF0000u));
+        }
+      } else {
       float f[4];
       const uint32_t kwa[4] = {kw.x, kw.y, kw.z, kw.w};
       const uint32_t vwa[4] = {vw.x, vw.y, vw.z, vw.w};
@@ -232,12 +248,18 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
           e4m3x4_to_f32(vwa[j], f);
         *reinterpret_cast<float4*>(&Vs[t * D + vv * 16 + j * 4]) = make_float4(f[0], f[1], f[2], f[3]);
       }
+      }
     }
+    };
+    if (p.kv_format == FP8KV_KV_BF16)
+      load_tile(std::integral_constant<int, D / 8>{});
+    else
+      load_tile(std::integral_constant<int, D / 16>{});
     const bool vflag = __syncthreads_or(vbad) != 0;  // the tile holds a non-finite V code
 
     // ------------------------------------------------------ scores (lane = token)
     // Compensated QK: products q*k are exact in FP32 (11-bit x 4-bit
-    // significands); they are summed in chunks of 8 and the chunk sums are
+    // significands; 11 x 8 for bf16 K); they are summed in chunks of 8 and the chunk sums are
     // combined with an error-free TwoSum into hi + lo, so the logit keeps
     // more than FP32 precision.  The base-2 exponent is then formed as
     // fma(hi, c, -m) + lo*c, which rounds only the small difference to the

@@ -49,7 +49,7 @@ class DeviceProblem:
             mode=mode, batch=p.B, q_max=p.q, num_q_heads=p.Hq, num_kv_heads=p.Hkv,
             head_dim=p.D, page_size=p.page_size, max_kv_len=max_kv_len, max_blocks=max_blocks,
             num_kv_blocks=int(kc.shape[0]), num_sms=num_sms, num_splits=num_splits, kernel=kernel, test_flags=test_flags,
-            kv_format=B.KV_E5M2 if getattr(p, "kv_format", "e4m3") == "e5m2" else B.KV_E4M3)
+            kv_format={"e4m3": B.KV_E4M3, "e5m2": B.KV_E5M2, "bf16": B.KV_BF16}[getattr(p, "kv_format", "e4m3")])
         self.plan = B.fp8kv_attn_plan(self.desc)
         self.workspace = torch.zeros(int(self.plan.workspace_bytes), dtype=torch.uint8, device=dev)
         self.k_scale_dev = self.v_scale_dev = None

@@ -90,6 +90,13 @@ extern "C" {
  * format of the kernels "DFlash2 E4M3 attention with FP32 state" replaces. */
 #define FP8KV_KV_E4M3 0
 #define FP8KV_KV_E5M2 1
+/* bf16 K/V (two bytes per element, little-endian; a token row is 2*head_dim
+ * bytes): the unquantised cache for A/B runs against the FP8 path
+ * ("DFlash2 E4M3 attention with FP32 state": the FP8 cache replaces a 16-bit
+ * one).  Served by the FP32 CUDA-core kernel only (FP8KV_KERNEL_GENERIC;
+ * asking for a tensor-core kernel gives FP8KV_EUNSUPPORTED).  The scales
+ * apply as for the FP8 formats (1.0 for an unscaled cache). */
+#define FP8KV_KV_BF16 2
 
 /* Split-kernel choice (desc.kernel; the plan records the one chosen). */
 #define FP8KV_KERNEL_AUTO 0

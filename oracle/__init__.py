@@ -189,7 +189,7 @@ class _Pinned:
         s.softmax_scale = p.softmax_scale
         s.k_scale = p.k_scale
         s.v_scale = p.v_scale
-        s.kv_format = 1 if getattr(p, "kv_format", "e4m3") == "e5m2" else 0
+        s.kv_format = {"e4m3": 0, "e5m2": 1, "bf16": 2}[getattr(p, "kv_format", "e4m3")]
         self.s = s
 
 

@@ -68,7 +68,7 @@ typedef struct {
   const int32_t* n_entries;      // sparse: [B]
   int64_t entry_stride;
   double softmax_scale, k_scale, v_scale;
-  int kv_format;  // cache byte format: 0 = E4M3 (E4M3FN), 1 = E5M2
+  int kv_format;  // cache format: 0 = E4M3 (E4M3FN) bytes, 1 = E5M2 bytes, 2 = bf16 pairs
   const uint32_t* entry_mask_hi; // sparse rows 8..15: [B][entry_stride], NULL for q <= 8
 } orc_problem;
 
@@ -129,7 +129,14 @@ ORC_API void orc_e5m2_table(double* out256) {
 }
 
 // The problem's cache byte decode.
-static inline double dec(const orc_problem* p, uint8_t b) { return p->kv_format == 1 ? orc_e5m2(b) : orc_e4m3(b); }
+ORC_API double orc_bf16(uint16_t h);
+
+// Element d of a K or V cache row: one E4M3 or E5M2 byte, or (kv_format 2) a
+// little-endian bf16 pair.
+static inline double dec(const orc_problem* p, const uint8_t* row, int d) {
+  if (p->kv_format == 2) return orc_bf16((uint16_t)(row[2 * d] | (row[2 * d + 1] << 8)));
+  return p->kv_format == 1 ? orc_e5m2(row[d]) : orc_e4m3(row[d]);
+}
 
 // IEEE binary16 bits -> value.
 ORC_API double orc_f16(uint16_t h) {
@@ -282,7 +289,7 @@ static void logits(const orc_problem* p, int b, int r, int h, const std::vector<
   for (size_t j = 0; j < toks.size(); ++j) {
     const uint8_t* kb = p->k_cache + toks[j].k_off;
     double dot = 0.0;
-    for (int d = 0; d < D; ++d) dot += qd[d] * dec(p, kb[d]);
+    for (int d = 0; d < D; ++d) dot += qd[d] * dec(p, kb, d);
     double sc = p->softmax_scale * p->k_scale;
 #if ORC_PLANT == 2
     sc = p->softmax_scale;  // planted: k_scale dropped
@@ -334,7 +341,7 @@ static void row_head_abs(const orc_problem* p, int b, int r, int h, double* out)
   for (size_t j = 0; j < toks.size(); ++j) {
     const double w = std::exp(z[j] - M) / S;
     const uint8_t* vb = p->v_cache + toks[j].v_off;
-    for (int d = 0; d < D; ++d) acc[d] += w * std::fabs(dec(p, vb[d]));
+    for (int d = 0; d < D; ++d) acc[d] += w * std::fabs(dec(p, vb, d));
   }
   for (int d = 0; d < D; ++d) out[d] = std::fabs(p->v_scale) * acc[d];
 }
@@ -366,14 +373,14 @@ static void row_head_logit_cond(const orc_problem* p, int b, int r, int h, doubl
     w[j] = std::exp(z[j] - M) / S;
     const uint8_t* kb = p->k_cache + toks[j].k_off;
     double s = 0.0;
-    for (int d = 0; d < D; ++d) s += std::fabs(orc_f16(qv[d]) * dec(p, kb[d]));
+    for (int d = 0; d < D; ++d) s += std::fabs(orc_f16(qv[d]) * dec(p, kb, d));
     a[j] = sc * s;
     const uint8_t* vb = p->v_cache + toks[j].v_off;
-    for (int d = 0; d < D; ++d) o[d] += w[j] * p->v_scale * dec(p, vb[d]);
+    for (int d = 0; d < D; ++d) o[d] += w[j] * p->v_scale * dec(p, vb, d);
   }
   for (size_t j = 0; j < toks.size(); ++j) {
     const uint8_t* vb = p->v_cache + toks[j].v_off;
-    for (int d = 0; d < D; ++d) out[d] += w[j] * a[j] * std::fabs(p->v_scale * dec(p, vb[d]) - o[d]);
+    for (int d = 0; d < D; ++d) out[d] += w[j] * a[j] * std::fabs(p->v_scale * dec(p, vb, d) - o[d]);
   }
 }
 
@@ -400,7 +407,7 @@ static void row_head(const orc_problem* p, int b, int r, int h, double* out) {
 #else
     const uint8_t* vb = p->v_cache + toks[j].v_off;
 #endif
-    for (int d = 0; d < D; ++d) acc[d] += w * dec(p, vb[d]);
+    for (int d = 0; d < D; ++d) acc[d] += w * dec(p, vb, d);
   }
   double vs = p->v_scale;
 #if ORC_PLANT == 5
@@ -432,7 +439,7 @@ static void row_head_split(const orc_problem* p, int b, int r, int h, int S_, do
       const double e = std::exp(z[j] - m[s]);
       l[s] += e;
       const uint8_t* vb = p->v_cache + toks[j].v_off;
-      for (int d = 0; d < D; ++d) num[(size_t)s * D + d] += e * dec(p, vb[d]);
+      for (int d = 0; d < D; ++d) num[(size_t)s * D + d] += e * dec(p, vb, d);
     }
   }
   double M = -std::numeric_limits<double>::infinity();
@@ -454,7 +461,7 @@ static int check(const orc_problem* p) {
   if (!p || p->B < 0 || p->q < 1 || p->Hq < 1 || p->Hkv < 1 || p->D < 1) return -1;
   if (p->Hq % p->Hkv) return -1;
   if (p->mode == 1 && (p->q > 16 || (p->q > 8 && !p->entry_mask_hi))) return -1;
-  if (p->kv_format != 0 && p->kv_format != 1) return -1;
+  if (p->kv_format < 0 || p->kv_format > 2) return -1;
   return 0;
 }
 

@@ -48,6 +48,8 @@ import torch
 E4M3_MAX = 448.0
 E5M2_MAX = 57344.0
 FMT_MAX = {"e4m3": E4M3_MAX, "e5m2": E5M2_MAX}
+BF16_POISON = {0x7F: (0xC0, 0x7F),  # the NaN poison as bf16: 0x7FC0
+               0x7E: (0x7F, 0x7F)}  # the largest-finite poison as bf16: 0x7F7F
 POISON_NAN = 0x7F      # E4M3 NaN
 POISON_MAX = 0x7E      # E4M3 +448: finite, so only true exclusion survives it
 
@@ -58,7 +60,7 @@ class Problem:
 
     Shapes (NHD page layout, D contiguous):
       q_fp16       [B][q][Hq][D]            torch.float16
-      k_cache      [num_blocks][P][Hkv][D]  torch.uint8 (E4M3 bytes)
+      k_cache      [num_blocks][P][Hkv][D]  torch.uint8 (E4M3/E5M2 bytes; bf16: [..][2D], LE pairs)
       v_cache      [num_blocks][P][Hkv][D]  torch.uint8
       block_table  [B][max_pages]           torch.int32   (dense)
       row_len      [B][q]                   torch.int32   (dense; 0 = dead row)
@@ -89,7 +91,7 @@ class Problem:
     entry_mask: Optional[torch.Tensor] = None
     n_entries: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
-    kv_format: str = "e4m3"       # cache byte format: "e4m3" (E4M3FN) or "e5m2"
+    kv_format: str = "e4m3"       # cache format: "e4m3" (E4M3FN), "e5m2" or "bf16"
     entry_mask_hi: Optional[torch.Tensor] = None  # sparse rows 8..15 (q > 8)
 
     @property
@@ -140,11 +142,25 @@ def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
     return y.to(torch.float8_e4m3fn).view(torch.uint8)
 
 
+def _poisoned(shape, poison: int, kv_format: str) -> torch.Tensor:
+    """A uint8 cache tensor filled with the poison code (bf16: its two-byte
+    counterpart, NaN for the NaN poison and the largest finite for 0x7E)."""
+    t = torch.full(shape, poison, dtype=torch.uint8)
+    if kv_format == "bf16":
+        lo, hi = BF16_POISON.get(poison, (poison, poison))
+        t[..., 0::2] = lo
+        t[..., 1::2] = hi
+    return t
+
+
 def quantize_fp8(x: torch.Tensor, scale: float, kv_format: str = "e4m3") -> torch.Tensor:
     """Cache bytes of x/scale in the given format (torch's RNE conversion
-    after clamping to the finite range)."""
+    after clamping to the finite range); bf16: two bytes per element, so the
+    last dimension doubles."""
     if kv_format == "e4m3":
         return quantize_e4m3(x, scale)
+    if kv_format == "bf16":
+        return (x / scale).to(torch.bfloat16).contiguous().view(torch.uint8)
     y = (x / scale).clamp_(-E5M2_MAX, E5M2_MAX)
     return y.to(torch.float8_e5m2).view(torch.uint8)
 
@@ -226,8 +242,9 @@ def make_dense(
         block_table[b, : pages[b]] = phys[off: off + pages[b]]
         off += pages[b]
 
-    k_cache = torch.full((num_blocks, page_size, Hkv, D), poison, dtype=torch.uint8)
-    v_cache = torch.full((num_blocks, page_size, Hkv, D), poison, dtype=torch.uint8)
+    Db = 2 * D if kv_format == "bf16" else D  # bytes of a token row
+    k_cache = _poisoned((num_blocks, page_size, Hkv, Db), poison, kv_format)
+    v_cache = _poisoned((num_blocks, page_size, Hkv, Db), poison, kv_format)
 
     def draw(b, which):
         return _gauss(_seed(seed, 2, b, which), (lens[b], Hkv, D), outliers)
@@ -240,8 +257,10 @@ def make_dense(
                 continue
             kmax = max(kmax, float(draw(b, 0).abs().max()))
             vmax = max(vmax, float(draw(b, 1).abs().max()))
-        ks = _f32(kmax / FMT_MAX[kv_format]) if kmax > 0 else 1.0
-        vs = _f32(vmax / FMT_MAX[kv_format]) if vmax > 0 else 1.0
+        ks = _f32(kmax / FMT_MAX.get(kv_format, 1.0)) if kmax > 0 else 1.0
+        vs = _f32(vmax / FMT_MAX.get(kv_format, 1.0)) if vmax > 0 else 1.0
+        if kv_format == "bf16":  # no quantisation scale
+            ks = vs = 1.0
         q_k, q_v = ks, vs
     elif value_mode == "direct":
         ks = _f32(k_scale)
@@ -259,8 +278,8 @@ def make_dense(
         full = L // page_size
         if full:
             ids = block_table[b, :full].long()
-            k_cache[ids] = kb[: full * page_size].view(full, page_size, Hkv, D)
-            v_cache[ids] = vb[: full * page_size].view(full, page_size, Hkv, D)
+            k_cache[ids] = kb[: full * page_size].view(full, page_size, Hkv, Db)
+            v_cache[ids] = vb[: full * page_size].view(full, page_size, Hkv, Db)
         rem = L - full * page_size
         if rem:
             pid = int(block_table[b, full])
@@ -319,27 +338,26 @@ def make_sparse(
     perm = torch.randperm(total, generator=_gen(seed, 11)).to(torch.int64)
     phys_of = (1 + perm).view(B, nmb)
 
-    k_cache = torch.empty((num_blocks, P, Hkv, D), dtype=torch.uint8)
-    v_cache = torch.empty((num_blocks, P, Hkv, D), dtype=torch.uint8)
-    k_cache[0] = poison
-    v_cache[0] = poison
+    Db = 2 * D if kv_format == "bf16" else D  # bytes of a token row
+    k_cache = _poisoned((num_blocks, P, Hkv, Db), poison, kv_format)
+    v_cache = _poisoned((num_blocks, P, Hkv, Db), poison, kv_format)
 
     def draw(b, which):
         return _gauss(_seed(seed, 12, b, which), (nmb * P, Hkv, D), outliers)
 
     kmax = max(float(draw(b, 0).abs().max()) for b in range(B))
     vmax = max(float(draw(b, 1).abs().max()) for b in range(B))
-    ks = _f32(kmax / FMT_MAX[kv_format])
-    vs = _f32(vmax / FMT_MAX[kv_format])
+    ks = _f32(kmax / FMT_MAX[kv_format]) if kv_format != "bf16" else 1.0
+    vs = _f32(vmax / FMT_MAX[kv_format]) if kv_format != "bf16" else 1.0
     for b in range(B):
         ids = phys_of[b]
-        k_cache[ids] = quantize_fp8(draw(b, 0), ks, kv_format).view(nmb, P, Hkv, D)
-        v_cache[ids] = quantize_fp8(draw(b, 1), vs, kv_format).view(nmb, P, Hkv, D)
+        k_cache[ids] = quantize_fp8(draw(b, 0), ks, kv_format).view(nmb, P, Hkv, Db)
+        v_cache[ids] = quantize_fp8(draw(b, 1), vs, kv_format).view(nmb, P, Hkv, Db)
         # tokens past the context in the last microblock are poisoned
         tail = nmb * P - L
         if tail:
-            k_cache[int(ids[-1]), P - tail:] = poison
-            v_cache[int(ids[-1]), P - tail:] = poison
+            k_cache[int(ids[-1]), P - tail:] = _poisoned((tail, Hkv, Db), poison, kv_format)
+            v_cache[int(ids[-1]), P - tail:] = _poisoned((tail, Hkv, Db), poison, kv_format)
 
     tbls, masks = [], []
     for b in range(B):
@@ -466,13 +484,15 @@ def make_problem(name: str, *, poison: int = POISON_NAN, seed: Optional[int] = N
 
 def attended_kv_bytes(p: Problem) -> int:
     """Attended-KV bytes: per request and KV head, the union of tokens any row
-    sees, times D bytes of K plus D bytes of V (E4M3)."""
+    sees, times the bytes of its K and V rows (D each for E4M3/E5M2, 2D for
+    bf16)."""
+    row = 2 * p.D if p.kv_format == "bf16" else p.D
     if p.mode == "dense":
         tot = 0
         for b in range(p.B):
             u = int(p.row_len[b].max()) if p.q > 0 else 0
             tot += u
-        return tot * p.Hkv * 2 * p.D
+        return tot * p.Hkv * 2 * row
     m = masks_any(p)
     tot = 0
     for b in range(p.B):
@@ -481,4 +501,4 @@ def attended_kv_bytes(p: Problem) -> int:
         for t in range(4):
             sel = (mb & (0x11111111 << t)) != 0
             tot += int(sel.sum())
-    return tot * p.Hkv * 2 * p.D
+    return tot * p.Hkv * 2 * row

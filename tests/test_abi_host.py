@@ -138,6 +138,17 @@ def test_sparse_rows_past_8_need_the_second_mask_words(B):
     assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == B.EINVAL
 
 
+def test_bf16_cache_takes_the_cuda_core_kernel(B):
+    plan = B.fp8kv_attn_plan(_desc(B, kv_format=B.KV_BF16))
+    assert plan.kernel == 1 and plan.kv_format == B.KV_BF16
+    for k in (2, 3):
+        with pytest.raises(B.Fp8kvError) as ei:
+            B.fp8kv_attn_plan(_desc(B, kv_format=B.KV_BF16, kernel=k))
+        assert ei.value.code == -2
+    with pytest.raises(B.Fp8kvError):
+        B.fp8kv_attn_plan(_desc(B, kv_format=3))
+
+
 def test_launch_workspace_and_revision(B):
     plan = B.fp8kv_attn_plan(_desc(B))
     a = _fake_args(B, plan, workspace_bytes=plan.workspace_bytes - 1)
@@ -274,5 +285,7 @@ def test_combine_lse_needs_its_outputs(B):
 def test_plan_records_the_cache_format(B):
     assert B.fp8kv_attn_plan(_desc(B)).kv_format == B.KV_E4M3
     assert B.fp8kv_attn_plan(_desc(B, kv_format=B.KV_E5M2)).kv_format == B.KV_E5M2
-    with pytest.raises(B.Fp8kvError):
-        B.fp8kv_attn_plan(_desc(B, kv_format=2))
+    assert B.fp8kv_attn_plan(_desc(B, kv_format=B.KV_BF16)).kv_format == B.KV_BF16
+    for bad in (3, -1):
+        with pytest.raises(B.Fp8kvError):
+            B.fp8kv_attn_plan(_desc(B, kv_format=bad))
