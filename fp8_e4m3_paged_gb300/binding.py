@@ -84,6 +84,12 @@ class Args(ctypes.Structure):
         ("out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("entry_mask_hi", ctypes.c_void_p),
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("k_new_stride_req", ctypes.c_int64), ("k_new_stride_token", ctypes.c_int64),
+        ("k_new_stride_head", ctypes.c_int64),
+        ("v_new_stride_req", ctypes.c_int64), ("v_new_stride_token", ctypes.c_int64),
+        ("v_new_stride_head", ctypes.c_int64),
+        ("n_new", ctypes.c_int32), ("new_dtype", ctypes.c_int32),
     ]
 
 
@@ -106,7 +112,7 @@ class CacheWriteArgs(ctypes.Structure):
         ("vc_stride_head", ctypes.c_int64),
         ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
         ("k_scale_dev", ctypes.c_void_p), ("v_scale_dev", ctypes.c_void_p),
-        ("status", ctypes.c_void_p),
+        ("status", ctypes.c_void_p), ("kv_format", ctypes.c_int32),
     ]
 
 
@@ -225,12 +231,14 @@ def make_args(*, q, k_cache, v_cache, out, workspace, softmax_scale: float,
               k_scale: float = 1.0, v_scale: float = 1.0,
               block_table=None, row_kv_len=None,
               entry_tbl=None, entry_mask=None, n_entries=None,
-              k_scale_dev=None, v_scale_dev=None, entry_mask_hi=None) -> Args:
+              k_scale_dev=None, v_scale_dev=None, entry_mask_hi=None, k_new=None, v_new=None) -> Args:
     """Fill an Args struct from torch CUDA tensors.
 
     k_cache / v_cache: uint8 tensors indexed [block][slot][kv_head][d] (any
     strides with d contiguous); q / out: fp16 [B][q_max][Hq][D] contiguous;
     workspace: a uint8 tensor of at least plan.workspace_bytes bytes.
+    k_new / v_new (fused write of a verify step's new tokens): fp16 or bf16
+    [B][n_new][Hkv][D], d contiguous.
     """
     a = Args()
     a.q = _ptr(q)
@@ -260,6 +268,14 @@ def make_args(*, q, k_cache, v_cache, out, workspace, softmax_scale: float,
     a.out = _ptr(out)
     a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if k_new is not None:
+        import torch
+
+        a.k_new, a.v_new = _ptr(k_new), _ptr(v_new)
+        a.k_new_stride_req, a.k_new_stride_token, a.k_new_stride_head = k_new.stride()[:3]
+        a.v_new_stride_req, a.v_new_stride_token, a.v_new_stride_head = v_new.stride()[:3]
+        a.n_new = k_new.shape[1]
+        a.new_dtype = DTYPE_F16 if k_new.dtype == torch.float16 else DTYPE_BF16
     return a
 
 
@@ -288,7 +304,7 @@ def fp8kv_attn_cache_write(args: CacheWriteArgs, stream: int = 0) -> None:
 
 def make_cache_write_args(*, k, v, slot_mapping, k_cache, v_cache, page_size: int,
                           k_scale: float = 1.0, v_scale: float = 1.0, k_scale_dev=None,
-                          v_scale_dev=None, status=None) -> CacheWriteArgs:
+                          v_scale_dev=None, status=None, kv_format: int = KV_E4M3) -> CacheWriteArgs:
     """Fill a CacheWriteArgs struct from torch CUDA tensors.
 
     k / v: float16 or bfloat16 [N][Hkv][D] (d contiguous); slot_mapping:
@@ -312,6 +328,7 @@ def make_cache_write_args(*, k, v, slot_mapping, k_cache, v_cache, page_size: in
     a.k_scale, a.v_scale = float(k_scale), float(v_scale)
     a.k_scale_dev, a.v_scale_dev = _ptr(k_scale_dev), _ptr(v_scale_dev)
     a.status = _ptr(status)
+    a.kv_format = kv_format
     return a
 
 

@@ -239,6 +239,29 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->k_scale_dev = a->k_scale_dev;
   p->v_scale_dev = a->v_scale_dev;
   p->out = reinterpret_cast<uint16_t*>(a->out);
+  p->n_new = 0;
+  p->k_new = p->v_new = nullptr;
+  if (a->n_new != 0) {
+    // fused write of the new tokens: dense FP8 caches, aligned rows
+    if (a->n_new < 0 || a->n_new > plan->max_kv_len || plan->mode != FP8KV_MODE_DENSE) return FP8KV_EINVAL;
+    if (plan->kv_format != FP8KV_KV_E4M3 && plan->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
+    if (a->new_dtype != FP8KV_DTYPE_F16 && a->new_dtype != FP8KV_DTYPE_BF16) return FP8KV_EINVAL;
+    if (!a->k_new || !a->v_new || !aligned(a->k_new, 16) || !aligned(a->v_new, 16)) return FP8KV_EINVAL;
+    const int64_t ns[6] = {a->k_new_stride_req, a->k_new_stride_token, a->k_new_stride_head,
+                           a->v_new_stride_req, a->v_new_stride_token, a->v_new_stride_head};
+    for (int64_t s : ns)
+      if (s < 0 || (s % 8) != 0) return FP8KV_EINVAL;
+    if (!a->k_scale_dev && !(a->k_scale > 0.f)) return FP8KV_EINVAL;
+    if (!a->v_scale_dev && !(a->v_scale > 0.f)) return FP8KV_EINVAL;
+    p->n_new = a->n_new;
+    p->new_dtype = a->new_dtype;
+    p->k_new = reinterpret_cast<const uint16_t*>(a->k_new);
+    p->v_new = reinterpret_cast<const uint16_t*>(a->v_new);
+    for (int i = 0; i < 3; ++i) {
+      p->kn_s[i] = ns[i];
+      p->vn_s[i] = ns[3 + i];
+    }
+  }
   char* ws = reinterpret_cast<char*>(a->workspace);
   p->status = reinterpret_cast<unsigned int*>(ws);
   p->partial = reinterpret_cast<float*>(ws + plan->partial_offset);
@@ -278,6 +301,7 @@ extern "C" int fp8kv_attn_cache_write(const fp8kv_cache_write_args* a, fp8kv_str
     return FP8KV_EINVAL;
   if (a->head_dim < 16 || a->head_dim > 1024 || (a->head_dim % 16) != 0) return FP8KV_EINVAL;
   if (a->dtype != FP8KV_DTYPE_F16 && a->dtype != FP8KV_DTYPE_BF16) return FP8KV_EINVAL;
+  if (a->kv_format != FP8KV_KV_E4M3 && a->kv_format != FP8KV_KV_E5M2) return FP8KV_EINVAL;
   if (a->num_tokens == 0) return FP8KV_OK;
   if (!a->k || !a->v || !a->slot_mapping || !a->k_cache || !a->v_cache) return FP8KV_EINVAL;
   if (!aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16))

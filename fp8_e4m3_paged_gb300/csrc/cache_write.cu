@@ -1,10 +1,11 @@
-// Cache write: new fp16 / bf16 K and V rows -> E4M3 bytes in the paged cache.
+// Cache write: new fp16 / bf16 K and V rows -> E4M3 (or E5M2) bytes in the
+// paged cache.
 //
-//   byte = E4M3(fp32(x) / scale)
+//   byte = E4M3(fp32(x) / scale)        (E5M2 likewise)
 //
 // with the division correctly rounded in FP32 and the conversion done by the
-// hardware's cvt.rn.satfinite.e4m3x2.f32 (round to nearest even, saturating
-// to +-448).  The quotient only matters through its E4M3 rounding, so the
+// hardware's cvt.rn.satfinite.e4m3x2.f32 / .e5m2x2.f32 (round to nearest
+// even, saturating to +-448 / +-57344).  The quotient only matters through its E4M3 rounding, so the
 // kernel multiplies by the reciprocal and divides exactly only where that
 // could change the code (see quot()).  This is the write path that fills the cache the attention
 // reads, with the layer's per-tensor scales ("Qwen4Exp: fp8_e4m3 main KV
@@ -21,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
+#include "fp8_encode.cuh"
 #include "internal.h"
 
 namespace fp8kv {
@@ -28,60 +30,10 @@ namespace {
 
 constexpr int kCwThreads = 256;
 
-// Four floats (memory order) -> four E4M3 bytes, little-endian in a word.
-// The instruction puts its first source in the upper byte of the pair.
-__device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x3) {
-  uint32_t w;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t}"
-      : "=r"(w)
-      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
-  return w;
-}
-
-// Two 2-byte elements (one 32-bit word) -> two floats.
-template <int DT>
-__device__ __forceinline__ float2 to_f32x2(uint32_t w) {
-  if (DT == FP8KV_DTYPE_F16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
-
-// x / s as far as its E4M3 code is concerned.  q = x * r with r = fl(1/s)
-// is within 2 fp32 ulps of the correctly rounded quotient fl(x/s) (one
-// rounding of r, one of the product).  The E4M3 code of a normal value is
-// decided by the 20 fp32 mantissa bits below its 3 kept bits against the
-// halfway pattern 0x80000, so when those bits of q are more than 4 ulps
-// from it, q and fl(x/s) lie strictly on the same side of the same
-// rounding boundary and convert to the same code.  Within 4 ulps of a
-// boundary, below the E4M3 normal range (2^-6), or for non-finite q the
-// exact quotient is computed.
-__device__ __forceinline__ float quot(float x, float s, float r) {
-  const float q = x * r;
-  const float aq = fabsf(q);
-  const uint32_t low = __float_as_uint(q) & 0xFFFFFu;
-  const bool exact = !(aq >= 0.015625f && aq <= 3.0e38f) || (low - 0x7FFFCu) <= 8u;
-  return exact ? __fdiv_rn(x, s) : q;
-}
-
-// 16 elements (two 16-byte words) / scale -> 16 E4M3 bytes.
-template <int DT>
-__device__ __forceinline__ uint4 quant16(const uint4 (&x)[2], float scale, float rcp) {
-  uint32_t in[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
-  uint32_t o[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 a = to_f32x2<DT>(in[2 * j]), b = to_f32x2<DT>(in[2 * j + 1]);
-    o[j] = e4m3x4(quot(a.x, scale, rcp), quot(a.y, scale, rcp), quot(b.x, scale, rcp), quot(b.y, scale, rcp));
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // One work item = CPT consecutive 16-element chunks of one (token, head), K
 // and V.  The slot of the next item is loaded one iteration ahead, so the
 // input loads never wait for it.
-template <int DT, int CPT>
+template <int DT, int CPT, int FMT>
 __global__ void __launch_bounds__(kCwThreads) cache_write_kernel(const fp8kv_cache_write_args a) {
   const float ks = a.k_scale_dev ? *a.k_scale_dev : a.k_scale;
   const float vs = a.v_scale_dev ? *a.v_scale_dev : a.v_scale;
@@ -121,8 +73,8 @@ __global__ void __launch_bounds__(kCwThreads) cache_write_kernel(const fp8kv_cac
     uint8_t* vd = a.v_cache + blk * a.vc_stride_block + off * a.vc_stride_token + h * a.vc_stride_head + c0 * 16;
 #pragma unroll
     for (int j = 0; j < CPT; ++j) {
-      *reinterpret_cast<uint4*>(kd + 16 * j) = quant16<DT>(kx[j], ks, kr);
-      *reinterpret_cast<uint4*>(vd + 16 * j) = quant16<DT>(vx[j], vs, vr);
+      *reinterpret_cast<uint4*>(kd + 16 * j) = quant16<DT, FMT>(kx[j], ks, kr);
+      *reinterpret_cast<uint4*>(vd + 16 * j) = quant16<DT, FMT>(vx[j], vs, vr);
     }
   }
 }
@@ -136,10 +88,14 @@ cudaError_t launch_cache_write(const fp8kv_cache_write_args& a, cudaStream_t st)
   if (e != cudaSuccess) return e;
   const bool two = (a.head_dim / 16) % 2 == 0;  // two chunks per item when the row splits evenly
   void (*fn)(const fp8kv_cache_write_args);
-  if (a.dtype == FP8KV_DTYPE_F16)
-    fn = two ? cache_write_kernel<FP8KV_DTYPE_F16, 2> : cache_write_kernel<FP8KV_DTYPE_F16, 1>;
+  constexpr int E4 = FP8KV_KV_E4M3, E5 = FP8KV_KV_E5M2, F16 = FP8KV_DTYPE_F16, BF16 = FP8KV_DTYPE_BF16;
+  const bool e5 = a.kv_format == E5;
+  if (a.dtype == F16)
+    fn = e5 ? (two ? cache_write_kernel<F16, 2, E5> : cache_write_kernel<F16, 1, E5>)
+            : (two ? cache_write_kernel<F16, 2, E4> : cache_write_kernel<F16, 1, E4>);
   else
-    fn = two ? cache_write_kernel<FP8KV_DTYPE_BF16, 2> : cache_write_kernel<FP8KV_DTYPE_BF16, 1>;
+    fn = e5 ? (two ? cache_write_kernel<BF16, 2, E5> : cache_write_kernel<BF16, 1, E5>)
+            : (two ? cache_write_kernel<BF16, 2, E4> : cache_write_kernel<BF16, 1, E4>);
   // one wave of resident CTAs (grid-stride loop over the items)
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kCwThreads, 0);

@@ -41,6 +41,11 @@ struct Params {
   const int32_t* entry_tbl;
   const uint32_t* entry_mask;
   const uint32_t* entry_mask_hi;  // sparse rows 8..15 (NULL with q_max <= 8)
+  // fused write of the new tokens (n_new = 0: none); strides in elements
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int64_t kn_s[3], vn_s[3];  // request, token, head
+  int32_t n_new, new_dtype;
   const int32_t* n_entries;
   int64_t entry_stride;
   // scales: logit factor = softmax_scale * k_scale * log2(e)

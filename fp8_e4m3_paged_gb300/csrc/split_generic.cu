@@ -23,6 +23,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "new_tokens.cuh"
 
 namespace fp8kv {
 namespace {
@@ -110,6 +111,18 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
   if (u0 >= u1) {
     for (int i = tid; i < RC; i += NT) ml_out[i] = make_float2(-INFINITY, 0.f);
     return;
+  }
+  // a verify step's new tokens in this partition, written before the tile
+  // loop reads them (which then bypasses L1: fresh = true)
+  const bool fresh = MODE == FP8KV_MODE_DENSE && p.n_new > 0;
+  if (fresh) {
+    if (u1 > U - p.n_new) {
+      if (p.kv_format == FP8KV_KV_E5M2)
+        write_new_tokens_and_fence<FP8KV_KV_E5M2>(p, b, g, U, u0, u1, tid, NT);
+      else
+        write_new_tokens_and_fence<FP8KV_KV_E4M3>(p, b, g, U, u0, u1, tid, NT);
+    }
+    __syncthreads();
   }
 
   // ---------------------------------------------------------- Q, row lengths
@@ -213,8 +226,13 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
       }
       uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
       if (ok) {
-        kw = __ldg(reinterpret_cast<const uint4*>(kp) + vv);
-        vw = __ldg(reinterpret_cast<const uint4*>(vp) + vv);
+        if (fresh) {
+          kw = __ldcg(reinterpret_cast<const uint4*>(kp) + vv);
+          vw = __ldcg(reinterpret_cast<const uint4*>(vp) + vv);
+        } else {
+          kw = __ldg(reinterpret_cast<const uint4*>(kp) + vv);
+          vw = __ldg(reinterpret_cast<const uint4*>(vp) + vv);
+        }
       }
       if constexpr (VPTL == D / 8) {
         // bf16: the upper half of an FP32 word, exact

@@ -76,6 +76,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "new_tokens.cuh"
 #include "tc_ptx.cuh"
 
 namespace fp8kv {
@@ -637,6 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc(const Params p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = mt.tmem;
+  if (MODE == FP8KV_MODE_DENSE && p.n_new > 0) {
+    // a verify step's new tokens in this partition: written by every thread
+    // before any copy of the pipeline can read them
+    if (u1 > U - p.n_new) write_new_tokens_and_fence<FMT>(p, b, g, U, u0, u1, tid, kThreads);
+    __syncthreads();
+  }
   volatile uint32_t* const abort_flag = &mt.abort;
   const uint32_t wlim = (p.test_flags & FP8KV_TEST_STALL_PIPELINE) ? kTestWaitLimit : kWaitLimit;
 

@@ -18,7 +18,7 @@ from . import binding as B
 class DeviceProblem:
     def __init__(self, p, *, device: str = "cuda", num_splits: int = 0, num_sms: int = 0,
                  kv_copies: int = 1, device_scales: bool = False, k_cache=None, v_cache=None,
-                 kernel: int = 0, test_flags: int = 0):
+                 kernel: int = 0, test_flags: int = 0, k_new=None, v_new=None):
         self.p = p
         dev = torch.device(device)
         self.q = p.q_fp16.to(dev).contiguous()
@@ -28,6 +28,9 @@ class DeviceProblem:
         self.k_caches = [kc.to(dev) for _ in range(kv_copies)]
         self.v_caches = [vc.to(dev) for _ in range(kv_copies)]
         self.out = torch.zeros_like(self.q)
+        # fused write of a verify step's new tokens ([B][n_new][Hkv][D] fp16/bf16)
+        self.k_new = None if k_new is None else k_new.to(dev).contiguous()
+        self.v_new = None if v_new is None else v_new.to(dev).contiguous()
         if p.mode == "dense":
             self.block_table = p.block_table.to(dev).contiguous()
             self.row_len = p.row_len.to(dev).contiguous()
@@ -67,7 +70,7 @@ class DeviceProblem:
             v_scale=0.0 if self.v_scale_dev is not None else p.v_scale,
             block_table=self.block_table, row_kv_len=self.row_len,
             entry_tbl=self.entry_tbl, entry_mask=self.entry_mask, n_entries=self.n_entries,
-            entry_mask_hi=self.entry_mask_hi,
+            entry_mask_hi=self.entry_mask_hi, k_new=self.k_new, v_new=self.v_new,
             k_scale_dev=self.k_scale_dev, v_scale_dev=self.v_scale_dev)
         return B.Call(self.plan, args)
 

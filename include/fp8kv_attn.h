@@ -194,6 +194,24 @@ typedef struct {
   size_t workspace_bytes;
   const uint32_t* entry_mask_hi; /* sparse with q_max > 8: [B][entry_stride] bits (4*(r-8) + t)
                                     of rows 8..15 (required there; ignored with q_max <= 8) */
+  /* Fused cache write (dense mode, E4M3/E5M2 caches; n_new = 0: none).  The
+   * last n_new positions of every request b -- U_b - n_new .. U_b - 1, with
+   * U_b its longest row_kv_len -- receive these new K and V rows, quantised
+   * in the cache's format with k_scale / v_scale exactly as
+   * fp8kv_attn_cache_write does, inside fp8kv_attn_split and before any of
+   * them is read: the verify step of speculative decoding writes its draft
+   * tokens and attends over them in one launch.  The caches must then be
+   * writable (k_cache / v_cache are written through).  Row j of request b,
+   * head h: k_new + b*k_new_stride_req + j*k_new_stride_token +
+   * h*k_new_stride_head (elements of new_dtype, d contiguous; strides
+   * multiples of 8, base 16-byte aligned).  A position whose block is out
+   * of range is not written and sets FP8KV_STATUS_BAD_BLOCK. */
+  const void* k_new;
+  const void* v_new;
+  int64_t k_new_stride_req, k_new_stride_token, k_new_stride_head;
+  int64_t v_new_stride_req, v_new_stride_token, v_new_stride_head;
+  int32_t n_new;                /* new tokens per request, 0..max_kv_len (each U_b >= n_new) */
+  int32_t new_dtype;            /* FP8KV_DTYPE_F16 (0) or FP8KV_DTYPE_BF16 (1) */
 } fp8kv_attn_args;
 
 /* Library revision (FP8KV_ATTN_REVISION). */
@@ -262,6 +280,8 @@ typedef struct {
   const float* k_scale_dev; /* optional device scalar, NULL = host */
   const float* v_scale_dev;
   uint32_t* status;       /* optional device word for FP8KV_STATUS_BAD_BLOCK, NULL = none */
+  int32_t kv_format;      /* FP8KV_KV_E4M3 (0, saturating to +-448) or FP8KV_KV_E5M2 (saturating to
+                             +-57344); round to nearest even either way */
 } fp8kv_cache_write_args;
 
 /* Launch the cache write on `stream`.  k, v and the caches must be 16-byte

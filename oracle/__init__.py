@@ -132,6 +132,10 @@ def load(plant: int = 0) -> ctypes.CDLL:
     lib.orc_cache_write.restype = ctypes.c_int
     lib.orc_cache_write.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, vp, vp, ctypes.c_float, ctypes.c_float,
                                                          vp, vp, vp, vp]
+    lib.orc_cache_write_fmt.restype = ctypes.c_int
+    lib.orc_cache_write_fmt.argtypes = lib.orc_cache_write.argtypes + [ctypes.c_int]
+    lib.orc_e5m2_encode.restype = ctypes.c_uint8
+    lib.orc_e5m2_encode.argtypes = [ctypes.c_float]
     _libs[plant] = lib
     return lib
 
@@ -279,13 +283,21 @@ def e4m3_encode(y, plant: int = 0) -> np.ndarray:
     return np.array([lib.orc_e4m3_encode(float(x)) for x in a], dtype=np.uint8).reshape(np.shape(y))
 
 
+def e5m2_encode(y, plant: int = 0) -> np.ndarray:
+    """E5M2 bytes of float32 values (round to nearest even, saturating to +-57344)."""
+    lib = load(plant)
+    a = np.asarray(y, dtype=np.float32).reshape(-1)
+    return np.array([lib.orc_e5m2_encode(float(x)) for x in a], dtype=np.uint8).reshape(np.shape(y))
+
+
 def bf16_value(bits: int, plant: int = 0) -> float:
     return load(plant).orc_bf16(bits)
 
 
 def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: float,
-                page_size: int, plant: int = 0) -> int:
-    """Write new tokens into E4M3 cache tensors in place (CPU).
+                page_size: int, plant: int = 0, kv_format: str = "e4m3") -> int:
+    """Write new tokens into E4M3 (or, kv_format "e5m2", E5M2) cache tensors
+    in place (CPU).
 
     k, v: float16 or bfloat16 [N][Hkv][D] (any strides, d contiguous);
     slot_mapping: int64 [N] (slot = block * page_size + offset, < 0 = skip);
@@ -303,10 +315,11 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: f
     ves = np.array(vb.stride()[:2], dtype=np.int64)
     kbs = np.array(k_cache.stride()[:3], dtype=np.int64)
     vbs = np.array(v_cache.stride()[:3], dtype=np.int64)
-    return load(plant).orc_cache_write(
+    return load(plant).orc_cache_write_fmt(
         N, Hkv, D, page_size, k_cache.shape[0], dtype, kb.data_ptr(), vb.data_ptr(),
         kes.ctypes.data, ves.ctypes.data, sm.data_ptr(), float(k_scale), float(v_scale),
-        k_cache.data_ptr(), v_cache.data_ptr(), kbs.ctypes.data, vbs.ctypes.data)
+        k_cache.data_ptr(), v_cache.data_ptr(), kbs.ctypes.data, vbs.ctypes.data,
+        {"e4m3": 0, "e5m2": 1}[kv_format])
 
 
 def attention_lse(p, threads: Optional[int] = None, plant: int = 0, **over):

@@ -189,6 +189,30 @@ ORC_API uint8_t orc_e4m3_encode(float y) {
   return (uint8_t)(sign | best);
 }
 
+// float -> E5M2 byte, from the format definition: the nearest finite code
+// (magnitudes 0x00..0x7B in increasing order; 0x7C is infinity, 0x7D..0x7F
+// NaN), ties to the code with an even mantissa, so values past the largest
+// finite 57344 (infinities included) saturate to it; NaN -> 0x7F.
+ORC_API uint8_t orc_e5m2_encode(float y) {
+  if (std::isnan(y)) return 0x7F;
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  const double a = std::fabs((double)y);
+  // past the largest finite value the nearest finite code is 57344 (an
+  // explicit test: far out, the distances to the two largest codes are
+  // equal in double precision and the even-code tie rule would pick 49152)
+  if (std::isinf(y) || a >= 57344.0) return (uint8_t)(sign | 0x7B);
+  int best = 0;
+  double best_d = std::numeric_limits<double>::infinity();
+  for (int c = 0; c <= 0x7B; ++c) {
+    const double d = std::fabs(a - orc_e5m2((uint8_t)c));
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best_d = d;
+      best = c;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
 // bfloat16 bits -> value (the upper half of a binary32).
 ORC_API double orc_bf16(uint16_t h) {
   uint32_t u = (uint32_t)h << 16;
@@ -205,10 +229,12 @@ ORC_API double orc_bf16(uint16_t h) {
 // with element strides (token, head); caches use byte strides (block, token,
 // head).  Slots whose block is outside [0, num_blocks) are skipped and
 // counted in the return value.
-ORC_API int orc_cache_write(int N, int Hkv, int D, int page_size, int num_blocks, int dtype,
-                            const uint16_t* k, const uint16_t* v, const int64_t* k_es, const int64_t* v_es,
-                            const int64_t* slot_mapping, float k_scale, float v_scale,
-                            uint8_t* k_cache, uint8_t* v_cache, const int64_t* k_bs, const int64_t* v_bs) {
+ORC_API int orc_cache_write_fmt(int N, int Hkv, int D, int page_size, int num_blocks, int dtype,
+                                const uint16_t* k, const uint16_t* v, const int64_t* k_es, const int64_t* v_es,
+                                const int64_t* slot_mapping, float k_scale, float v_scale,
+                                uint8_t* k_cache, uint8_t* v_cache, const int64_t* k_bs, const int64_t* v_bs,
+                                int kv_format) {
+  uint8_t (*enc)(float) = kv_format == 1 ? orc_e5m2_encode : orc_e4m3_encode;
   int bad = 0;
   for (int n = 0; n < N; ++n) {
     const int64_t slot = slot_mapping[n];
@@ -229,11 +255,20 @@ ORC_API int orc_cache_write(int N, int Hkv, int D, int page_size, int num_blocks
         const uint16_t vb = v[n * v_es[0] + h * v_es[1] + d];
         const float kx = (float)(dtype == 0 ? orc_f16(kb) : orc_bf16(kb));
         const float vx = (float)(dtype == 0 ? orc_f16(vb) : orc_bf16(vb));
-        k_cache[blk * k_bs[0] + off * k_bs[1] + h * k_bs[2] + d] = orc_e4m3_encode(kx / k_scale);
-        v_cache[blk * v_bs[0] + off * v_bs[1] + h * v_bs[2] + d] = orc_e4m3_encode(vx / v_scale);
+        k_cache[blk * k_bs[0] + off * k_bs[1] + h * k_bs[2] + d] = enc(kx / k_scale);
+        v_cache[blk * v_bs[0] + off * v_bs[1] + h * v_bs[2] + d] = enc(vx / v_scale);
       }
   }
   return bad;
+}
+
+// The E4M3 cache write (kv_format 0).
+ORC_API int orc_cache_write(int N, int Hkv, int D, int page_size, int num_blocks, int dtype,
+                            const uint16_t* k, const uint16_t* v, const int64_t* k_es, const int64_t* v_es,
+                            const int64_t* slot_mapping, float k_scale, float v_scale,
+                            uint8_t* k_cache, uint8_t* v_cache, const int64_t* k_bs, const int64_t* v_bs) {
+  return orc_cache_write_fmt(N, Hkv, D, page_size, num_blocks, dtype, k, v, k_es, v_es, slot_mapping, k_scale,
+                             v_scale, k_cache, v_cache, k_bs, v_bs, 0);
 }
 
 // ------------------------------------------------------- visible token set

@@ -7,8 +7,9 @@ it returns.
 Shape of a write: N new tokens of Hkv heads x D, fp16 or bf16, laid out as a
 paged allocator hands them out -- consecutive tokens fill a page, pages are
 physical blocks in a random order.  Values are N(0, std) with a few large
-outliers (so some codes saturate); ``edge=True`` mixes in exact E4M3
-midpoints (times the scale), signed zeros, values far below the smallest
+outliers (so some codes saturate); ``edge=True`` mixes in exact midpoints
+of the target format's codes (E4M3, or E5M2 with ``edge_format``; times the
+scale), signed zeros, values far below the smallest
 subnormal, infinities and NaN.  Some tokens are padding (slot -1) and some
 name a block beyond the pool.
 """
@@ -43,17 +44,26 @@ class CacheWriteProblem:
                 torch.full(shape, self.poison, dtype=torch.uint8))
 
 
-def _edge_values(n: int, scale: float, g: torch.Generator) -> torch.Tensor:
+def _edge_values(n: int, scale: float, g: torch.Generator, fmt: str = "e4m3") -> torch.Tensor:
     # magnitudes of the format's finite codes and the midpoints between
-    # neighbours, built from the bit layout (1 sign, 4 exponent, 3 mantissa)
+    # neighbours, built from the bit layout (E4M3: 1 sign, 4 exponent, 3
+    # mantissa, no infinity; E5M2: 1 sign, 5 exponent, 2 mantissa, exponent
+    # 31 for infinities and NaNs)
     mags = []
-    for e in range(16):
-        for m in range(8):
-            if e == 15 and m == 7:
-                continue
-            mags.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    if fmt == "e4m3":
+        for e in range(16):
+            for m in range(8):
+                if e == 15 and m == 7:
+                    continue
+                mags.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+        top = [448.0, 460.0]
+    else:
+        for e in range(31):
+            for m in range(4):
+                mags.append(m * 2.0 ** -16 if e == 0 else (1 + m / 4) * 2.0 ** (e - 15))
+        top = [57344.0, 61440.0]
     mids = [(a + b) / 2 for a, b in zip(mags[:-1], mags[1:])]
-    specials = [0.0, -0.0, 1e-12, -1e-12, 448.0, 460.0, 1e9, float("inf"), float("-inf"), float("nan")]
+    specials = [0.0, -0.0, 1e-12, -1e-12] + top + [1e9, float("inf"), float("-inf"), float("nan")]
     pool = torch.tensor(mags + mids + specials, dtype=torch.float64) * scale
     idx = torch.randint(0, pool.numel(), (n,), generator=g)
     sign = torch.where(torch.rand(n, generator=g) < 0.5, -1.0, 1.0).to(torch.float64)
@@ -64,7 +74,7 @@ def make_cache_write(N: int, Hkv: int, D: int, page_size: int, num_blocks: int, 
                      dtype=torch.float16, seed: int = 0, std: float = 1.0,
                      k_scale: float = 0.0078125, v_scale: float = 0.015625,
                      pad_fraction: float = 0.05, bad_slots: int = 2, edge: bool = False,
-                     poison: int = 0x5A) -> CacheWriteProblem:
+                     poison: int = 0x5A, edge_format: str = "e4m3") -> CacheWriteProblem:
     g = torch.Generator().manual_seed(seed)
     pages = (N + page_size - 1) // page_size
     assert pages <= num_blocks, "pool too small for the tokens"
@@ -83,7 +93,7 @@ def make_cache_write(N: int, Hkv: int, D: int, page_size: int, num_blocks: int, 
             if n_e == 0:
                 continue
             pos = torch.randperm(t.numel(), generator=g)[:n_e]
-            t.view(-1)[pos] = _edge_values(n_e, sc, g)
+            t.view(-1)[pos] = _edge_values(n_e, sc, g, edge_format)
     k = k.to(dtype)
     v = v.to(dtype)
     perm = torch.randperm(num_blocks, generator=g)[:pages].to(torch.int64)

@@ -149,6 +149,34 @@ def test_bf16_cache_takes_the_cuda_core_kernel(B):
         B.fp8kv_attn_plan(_desc(B, kv_format=3))
 
 
+@pytest.mark.parametrize("kw,plan_kw", [
+    (dict(n_new=-1), {}),
+    (dict(n_new=131073), {}),                                   # more than max_kv_len
+    (dict(n_new=8, k_new=None), {}),                            # rows missing
+    (dict(n_new=8, k_new=(1 << 20) + 8), {}),                   # misaligned
+    (dict(n_new=8, k_new_stride_token=100), {}),                # stride not a multiple of 8
+    (dict(n_new=8, new_dtype=2), {}),
+    (dict(n_new=8), dict(kv_format=2)),                         # bf16 cache: nothing to quantise to
+    (dict(n_new=8, k_scale=0.0), {}),
+])
+def test_fused_write_validation(B, kw, plan_kw):
+    plan = B.fp8kv_attn_plan(_desc(B, **plan_kw))
+    fake = 1 << 20
+    base = dict(k_new=fake, v_new=fake, k_new_stride_req=8 * 256, k_new_stride_token=256, k_new_stride_head=256,
+                v_new_stride_req=8 * 256, v_new_stride_token=256, v_new_stride_head=256, new_dtype=0)
+    base.update(kw)
+    a = _fake_args(B, plan, **base)
+    assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == B.EINVAL
+
+
+def test_fused_write_needs_dense_mode(B):
+    plan = B.fp8kv_attn_plan(_desc(B, mode=1, page_size=4, q_max=4, max_kv_len=0, max_blocks=64))
+    fake = 1 << 20
+    a = _fake_args(B, plan, block_table=None, row_kv_len=None, entry_tbl=fake, entry_mask=fake, n_entries=fake,
+                   entry_stride=64, n_new=4, k_new=fake, v_new=fake)
+    assert B.lib.fp8kv_attn_split(ctypes.byref(plan), ctypes.byref(a), None) == B.EINVAL
+
+
 def test_launch_workspace_and_revision(B):
     plan = B.fp8kv_attn_plan(_desc(B))
     a = _fake_args(B, plan, workspace_bytes=plan.workspace_bytes - 1)
@@ -191,6 +219,7 @@ def _cw(B, **kw):
     dict(page_size=0), dict(num_kv_blocks=0), dict(dtype=2), dict(k=0), dict(slot_mapping=0),
     dict(v_cache=0), dict(k=0x10008), dict(k_stride_token=3), dict(v_stride_head=-8),
     dict(kc_stride_token=8), dict(vc_stride_block=-16), dict(k_scale=0.0), dict(v_scale=float("nan")),
+    dict(kv_format=2), dict(kv_format=-1),
 ])
 def test_cache_write_rejects_bad_arguments(B, bad):
     assert B.lib.fp8kv_attn_cache_write(ctypes.byref(_cw(B, **bad)), None) == B.EINVAL

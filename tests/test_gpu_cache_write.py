@@ -32,7 +32,7 @@ def _lib():
     oracle.build()
 
 
-def _gpu_write(p, kc_cpu, vc_cpu, *, strided_in=False, device_scales=False, head_slice=None):
+def _gpu_write(p, kc_cpu, vc_cpu, *, strided_in=False, device_scales=False, head_slice=None, fmt="e4m3"):
     from fp8_e4m3_paged_gb300 import binding as B
 
     dev = torch.device("cuda")
@@ -56,25 +56,30 @@ def _gpu_write(p, kc_cpu, vc_cpu, *, strided_in=False, device_scales=False, head
     a = B.make_cache_write_args(k=k, v=v, slot_mapping=slots, k_cache=kc, v_cache=vc,
                                 page_size=p.page_size, k_scale=0.0 if device_scales else p.k_scale,
                                 v_scale=0.0 if device_scales else p.v_scale,
-                                k_scale_dev=ks, v_scale_dev=vs, status=status)
+                                k_scale_dev=ks, v_scale_dev=vs, status=status,
+                                kv_format=B.KV_E5M2 if fmt == "e5m2" else B.KV_E4M3)
     B.fp8kv_attn_cache_write(a, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     return kc_full.cpu(), vc_full.cpu(), int(status.item())
 
 
-def _oracle_write(p, kc_cpu, vc_cpu, head_slice=None):
+def _oracle_write(p, kc_cpu, vc_cpu, head_slice=None, fmt="e4m3"):
     kc, vc = kc_cpu.clone(), vc_cpu.clone()
     kv = kc if head_slice is None else kc[:, :, head_slice, :]
     vv = vc if head_slice is None else vc[:, :, head_slice, :]
-    bad = oracle.cache_write(p.k, p.v, p.slots, kv, vv, p.k_scale, p.v_scale, p.page_size)
+    bad = oracle.cache_write(p.k, p.v, p.slots, kv, vv, p.k_scale, p.v_scale, p.page_size, kv_format=fmt)
     return kc, vc, bad
 
 
-def _same_bytes(got, ref):
-    """Equal bytes, except that a NaN code may be either NaN code."""
+def _same_bytes(got, ref, fmt="e4m3"):
+    """Equal bytes, except that a NaN code may be any NaN code of the format."""
     g, r = got.numpy(), ref.numpy()
-    nan_g = (g & 0x7F) == 0x7F
-    nan_r = (r & 0x7F) == 0x7F
+    if fmt == "e5m2":
+        nan_g = ((g & 0x7C) == 0x7C) & ((g & 0x03) != 0)
+        nan_r = ((r & 0x7C) == 0x7C) & ((r & 0x03) != 0)
+    else:
+        nan_g = (g & 0x7F) == 0x7F
+        nan_r = (r & 0x7F) == 0x7F
     assert np.array_equal(nan_g, nan_r), "NaN codes differ in position"
     diff = (g != r) & ~nan_r
     assert not diff.any(), f"{int(diff.sum())} bytes differ, first at {np.argwhere(diff)[0].tolist()}"
@@ -103,6 +108,23 @@ def test_cache_write_edge_values(dtype):
     kr, vr, _ = _oracle_write(p, kc0, vc0)
     _same_bytes(kg, kr)
     _same_bytes(vg, vr)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("edge", [False, True])
+def test_e5m2_cache_write_matches_oracle(D, dtype, edge):
+    """The legacy E5M2 cache: byte-exact against the oracle's encoder, with
+    calibrated scales, exact E5M2 midpoints, saturation, signed zeros,
+    infinities and NaN."""
+    p = make_cache_write(N=150, Hkv=2, D=D, page_size=16, num_blocks=16, dtype=dtype, seed=D + 7,
+                         k_scale=0.0071, v_scale=3.3, std=200.0, edge=edge, edge_format="e5m2")
+    kc0, vc0 = p.empty_caches()
+    kg, vg, st = _gpu_write(p, kc0, vc0, fmt="e5m2")
+    kr, vr, bad = _oracle_write(p, kc0, vc0, fmt="e5m2")
+    _same_bytes(kg, kr, "e5m2")
+    _same_bytes(vg, vr, "e5m2")
+    assert bad == 2 and st == 1
 
 
 def test_cache_write_strides_and_device_scales():
