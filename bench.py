@@ -147,7 +147,7 @@ def run_ours(args):
     kv_bytes = p.k_cache.numel() + p.v_cache.numel()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     copies = max(2, math.ceil(3 * l2 / max(kv_bytes, 1)) + 1) if args.copies == 0 else args.copies
-    dp = DeviceProblem(p, kv_copies=copies)
+    dp = DeviceProblem(p, kv_copies=copies, kernel=args.kernel)
     torch.cuda.synchronize()
 
     s = torch.cuda.Stream()
@@ -911,6 +911,9 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reqs", type=int, default=0, help="c4 only: the first N of its 64 requests")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="split kernel: 0 = the planner's choice, 1 CUDA cores, 2 tcgen05 query rows, "
+                         "3 tcgen05 small group")
     ap.add_argument("--kv-format", choices=["e4m3", "e5m2", "bf16"], default="e4m3",
                     help="cache format (bf16: the unquantised cache, for A/B against the FP8 path)")
     ap.add_argument("--op", choices=["attention", "cache_write", "dcp_merge", "select_entries"], default="attention")

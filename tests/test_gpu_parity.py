@@ -3,7 +3,7 @@
 Every named workload runs through fp8kv_attn_plan / _split / _combine on
 cuda:0 and is compared element by element with the oracle on the same seeded
 bytes (tests/_check.py: rel L2 <= 5e-4, <= 4 fp16 ulps, no NaN/Inf), every
-output element in full, including the 1.76 GB batched decode workload.  Edge cases: forced split counts, graph
+output element in full, including the 1.39 GB batched decode workload.  Edge cases: forced split counts, graph
 replay with live lengths 8 -> 5 -> 0, bitwise determinism across replays,
 NaN and 448 poisoning of padding / unused slots, dead rows, device-side
 scales, interleaved K/V strides, out-of-range block ids and lengths.
@@ -98,7 +98,7 @@ def test_poisoned_padding(name, poison):
 
 @pytest.mark.parametrize("kernel,floor_elements", [(0, 2), (1, 1)])
 def test_c4_full(kernel, floor_elements):
-    """64 independent decode requests (1.76 GB of cache, 1 % outliers x20):
+    """64 independent decode requests (1.39 GB of attended KV, 1 % outliers x20):
     every query vector against the oracle, in the bench's launch config
     (kernel 0: the planner's choice, the small-group tensor-core kernel) and
     on the CUDA-core kernel.  The x20 outliers make some outputs cancel far
