@@ -89,18 +89,21 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
   P.kv_format = d->kv_format;
   P.test_flags = d->test_flags;
 
-  // Kernel choice for D = 128 or 256: up to 16 query vectors per (request,
-  // KV head) -- decode and small verify groups -- the transposed tcgen05
-  // kernel (tokens as the MMA rows, so its softmax works on 128 tokens at a
-  // time whatever the group size); more, the tcgen05 kernel with the query
-  // vectors as the MMA rows (up to 64 per CTA).  D = 64: the FP32 CUDA-core
-  // kernel, which also serves every shape on request.
+  // Kernel choice for D = 128 or 256: up to 8 query vectors per (request,
+  // KV head) -- decode with GQA -- the transposed tcgen05 kernel (tokens as
+  // the MMA rows); more, the tcgen05 kernel with the query vectors as the
+  // MMA rows (up to 64 per CTA).  Measured over contexts of 1K..64K tokens:
+  // with 4 or 8 vectors the two are within ~5 %, with 12 or 16 the
+  // query-row kernel is 30-60 % faster (the transposed kernel's softmax then
+  // carries 16 columns per token); the transposed kernel still takes up to 16
+  // on request.  D = 64 and bf16 caches: the FP32 CUDA-core kernel, which
+  // also serves every shape on request.
   const bool tc_dims = P.head_dim == 128 || P.head_dim == 256;
   int kind = d->kernel;
   if (kind == FP8KV_KERNEL_AUTO)
     kind = (!tc_dims || d->kv_format == FP8KV_KV_BF16)
                ? FP8KV_KERNEL_GENERIC
-               : (P.rows <= kTcSmallRows ? FP8KV_KERNEL_TC_SMALL : FP8KV_KERNEL_TC);
+               : (P.rows <= kTcSmallAutoRows ? FP8KV_KERNEL_TC_SMALL : FP8KV_KERNEL_TC);
   int tile, ctas_per_sm, max_part_tiles;
   if (kind == FP8KV_KERNEL_TC || kind == FP8KV_KERNEL_TC_SMALL) {
     const bool small = kind == FP8KV_KERNEL_TC_SMALL;

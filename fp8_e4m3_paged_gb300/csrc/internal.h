@@ -93,6 +93,7 @@ int generic_smem_bytes(int D, int row_chunk);
 // Tensor-core path: shared-memory bytes (D = 128 or 256), threads, tile size.
 int tc_smem_bytes(int D, bool small_group);
 constexpr int kTcSmallRows = 16;     // query vectors per CTA of the small-group kernel
+constexpr int kTcSmallAutoRows = 8;  // the planner's own choice of it: groups up to this size
 constexpr int kTcThreads = 480;
 constexpr int kTcTileTokens = 64;
 constexpr int kTcRows = 64;
