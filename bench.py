@@ -147,7 +147,17 @@ def run_ours(args):
     kv_bytes = p.k_cache.numel() + p.v_cache.numel()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     copies = max(2, math.ceil(3 * l2 / max(kv_bytes, 1)) + 1) if args.copies == 0 else args.copies
-    dp = DeviceProblem(p, kv_copies=copies, kernel=args.kernel)
+    k_new = v_new = None
+    if args.new_tokens:
+        # the verify step writes its draft tokens itself (fused cache write):
+        # fp16 rows for the last new_tokens positions of every request
+        if p.mode != "dense" or args.kv_format == "bf16":
+            raise SystemExit("--new-tokens: dense FP8 caches only")
+        g = torch.Generator().manual_seed(11)
+        shape = (p.B, args.new_tokens, p.Hkv, p.D)
+        k_new = torch.randn(shape, generator=g).to(torch.float16)
+        v_new = torch.randn(shape, generator=g).to(torch.float16)
+    dp = DeviceProblem(p, kv_copies=copies, kernel=args.kernel, k_new=k_new, v_new=v_new)
     torch.cuda.synchronize()
 
     s = torch.cuda.Stream()
@@ -278,6 +288,7 @@ def run_ours(args):
             "workload": f"{args.workload}: {WORKLOAD_DESC.get(args.workload, '')}",
             "attended_kv_bytes_per_step": bytes_step,
             "kv_format": args.kv_format,
+            "fused_new_tokens": args.new_tokens,
             "kernel": {1: "generic (CUDA cores)", 2: "tcgen05 (query rows)",
                        3: "tcgen05 small group (tokens as rows)"}.get(dp.plan.kernel, str(dp.plan.kernel)),
             "num_splits": dp.plan.num_splits,
@@ -350,6 +361,9 @@ def run_e2e(p, dp, args, s, bytes_step):
     if p.mode == "dense":
         host["bt"] = p.block_table.pin_memory()
         host["rl"] = p.row_len.pin_memory()
+        if dp.k_new is not None:
+            host["kn"] = dp.k_new.cpu().pin_memory()
+            host["vn"] = dp.v_new.cpu().pin_memory()
     else:
         host["et"] = p.entry_tbl.pin_memory()
         host["em"] = p.entry_mask.pin_memory()
@@ -358,6 +372,8 @@ def run_e2e(p, dp, args, s, bytes_step):
     dev = {"q": dp.q, "k": dp.k_caches[0], "v": dp.v_caches[0]}
     if p.mode == "dense":
         dev["bt"], dev["rl"] = dp.block_table, dp.row_len
+        if dp.k_new is not None:
+            dev["kn"], dev["vn"] = dp.k_new, dp.v_new
     else:
         dev["et"], dev["em"], dev["ne"] = dp.entry_tbl, dp.entry_mask, dp.n_entries
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -911,6 +927,9 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reqs", type=int, default=0, help="c4 only: the first N of its 64 requests")
+    ap.add_argument("--new-tokens", type=int, default=0,
+                    help="dense verify: the step also writes this many new tokens per request into the "
+                         "cache inside the split launch (fused cache write)")
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
                     help="split kernel: 0 = the planner's choice, 1 CUDA cores, 2 tcgen05 query rows, "
                          "3 tcgen05 small group")
