@@ -182,6 +182,7 @@ int fp8kv::build_params(const fp8kv_attn_plan_t* plan, const fp8kv_attn_args* a,
   p->n_row_chunks = plan->row_chunk > 0 ? (plan->rows + plan->row_chunk - 1) / plan->row_chunk : 0;
   p->S = plan->num_splits;
   p->page_size = plan->page_size;
+  p->page_div = plan->page_size >= 2 ? ~0ull / (uint64_t)plan->page_size + 1 : 0ull;
   p->max_kv_len = plan->max_kv_len;
   p->max_blocks = plan->max_blocks;
   p->num_kv_blocks = plan->num_kv_blocks;

@@ -27,6 +27,11 @@ struct Params {
   // problem
   int32_t mode, B, q_max, Hq, Hkv, D, G, rows, row_chunk, n_row_chunks, S;
   int32_t page_size, max_kv_len, max_blocks, num_kv_blocks;
+  // ceil(2^64 / page_size) (page_size >= 2; 0 for 1): the split kernels
+  // divide token indices by the page size with one multiply-high (Lemire,
+  // Kaser and Kurz, "Faster remainder by direct computation", 2019: exact for
+  // every numerator below 2^32 because 64 >= 32 + ceil(log2(page_size)))
+  uint64_t page_div;
   int32_t kv_format;  // FP8KV_KV_E4M3 or FP8KV_KV_E5M2
   int32_t test_flags; // FP8KV_TEST_* (0 in production)
   int32_t min_part;   // shortest partition: tokens (dense) or entries (sparse), 0 = none

@@ -342,11 +342,18 @@ struct TilePages {
   int bid;  // this lane's page
 };
 
+// The page of token `tok` (0 <= tok < 2^31): a multiply-high by the host's
+// rounded-up reciprocal instead of an integer division, whose long dependent
+// sequence paced the producer loop.
+__device__ __forceinline__ int page_of(const Params& p, int tok) {
+  return p.page_size == 1 ? tok : (int)__umul64hi(p.page_div, (unsigned long long)(unsigned)tok);
+}
+
 __device__ __forceinline__ TilePages fetch_pages(const Params& p, int b, int u0, int u1, int i, int lane) {
   TilePages tp;
   const int tok0 = u0 + i * kT;
-  tp.page0 = tok0 / p.page_size;
-  const int npages = tok0 < u1 ? (min(u1, tok0 + kT) - 1) / p.page_size - tp.page0 + 1 : 0;
+  tp.page0 = page_of(p, tok0);
+  const int npages = tok0 < u1 ? page_of(p, min(u1, tok0 + kT) - 1) - tp.page0 + 1 : 0;
   tp.bid = lane < npages ? p.block_table[(int64_t)b * p.bt_stride + tp.page0 + lane] : -1;
   return tp;
 }
@@ -365,7 +372,7 @@ __device__ __forceinline__ uint64_t copy_rows_dense(const Params& p, const uint8
   while (t < kT) {
     const int tok = u0 + i * kT + t;
     if (tok >= u1) break;
-    const int page = tok / p.page_size, slot_in = tok % p.page_size;
+    const int page = page_of(p, tok), slot_in = tok - page * p.page_size;
     const int dp = page - page0;
     const int blk = dp < 32 ? pblk[dp] : p.block_table[(int64_t)b * p.bt_stride + page];
     const int run = min(kT - t, min(p.page_size - slot_in, u1 - tok));
@@ -404,12 +411,12 @@ __device__ __forceinline__ uint64_t copy_tokens_dense(const Params& p, const uin
     const int tok = u0 + i * kT + t;
     bool ok = false;
     if (tok < u1) {
-      const int page = tok / p.page_size;
+      const int page = page_of(p, tok);
       const int dp = page - page0;
       const int blk = dp < 32 ? pblk[dp] : p.block_table[(int64_t)b * p.bt_stride + page];
       if (blk >= 0 && blk < p.num_kv_blocks) {
         ok = true;
-        copy_row_async<D>(dst + t * D, cache + blk * sb + (tok % p.page_size) * st + g * sh);
+        copy_row_async<D>(dst + t * D, cache + blk * sb + (tok - page * p.page_size) * st + g * sh);
       } else if (report) {
         set_status(p.status, FP8KV_STATUS_BAD_BLOCK);
       }

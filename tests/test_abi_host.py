@@ -10,6 +10,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -318,3 +319,23 @@ def test_plan_records_the_cache_format(B):
     for bad in (3, -1):
         with pytest.raises(B.Fp8kvError):
             B.fp8kv_attn_plan(_desc(B, kv_format=bad))
+
+
+def test_page_division_identity():
+    """The split kernels take a token's page as the high word of
+    page_div * token with page_div = ceil(2^64 / page_size) (the host writes
+    ~0 / page_size + 1).  Lemire, Kaser and Kurz ("Faster remainder by direct
+    computation", 2019) prove it exact for every numerator below 2^32 when
+    64 >= 32 + ceil(log2(page_size)); checked here on divisors and numerators
+    chosen around the multiples where a truncated reciprocal would fail."""
+    rng = np.random.default_rng(5)
+    divisors = list(range(2, 300)) + [1728, 3296, 4099, 65536, 1000003, 2**31 - 1]
+    divisors += [int(x) for x in rng.integers(2, 2**31, 200)]
+    for d in divisors:
+        c = (2**64 - 1) // d + 1
+        ns = [0, 1, d - 1, d, d + 1, 2**31 - 1, 2**32 - 1]
+        ns += [k * d + e for k in (2, 3, 1000, (2**32 - 1) // d) for e in (-1, 0, 1)]
+        ns += [int(x) for x in rng.integers(0, 2**32, 50)]
+        for n in ns:
+            if 0 <= n < 2**32:
+                assert (c * n) >> 64 == n // d, (d, n)

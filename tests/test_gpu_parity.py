@@ -181,6 +181,21 @@ def test_shapes_dense(D, q, Hq, Hkv):
     compare(got, oracle.attention(p), what=f"D={D} q={q} Hq={Hq} Hkv={Hkv}")
 
 
+@pytest.mark.parametrize("page_size", [1, 2, 3, 64, 97, 1000, 4099])
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_page_sizes(page_size, kernel):
+    """Token -> (page, slot) on the tensor-core kernels, which divide by the
+    page size with a multiply-high: page size 1 (its own branch), powers of
+    two, odd sizes, and pages longer than a whole partition."""
+    p = make_dense(B=2, q=2, Hq=8, Hkv=2, D=128, page_size=page_size, lens=[700, 1333],
+                   seed=900 + page_size + kernel)
+    dp = _dp(p, kernel=kernel)
+    assert dp.plan.kernel == kernel
+    got = _run(dp)
+    compare(got, oracle.attention(p), what=f"page {page_size} kernel {kernel}")
+    assert dp.status() == 0
+
+
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("q,Hq,Hkv", [(1, 4, 1), (4, 24, 2), (8, 8, 4)])
 def test_shapes_sparse(D, q, Hq, Hkv):
