@@ -114,7 +114,7 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
     P.block_threads = kTcThreads;
     P.smem_bytes = tc_smem_bytes(P.head_dim, small);
     ctas_per_sm = 1;
-    max_part_tiles = kTcMaxPartTiles;
+    max_part_tiles = small ? kTcSmallMaxPartTiles : kTcMaxPartTiles;
   } else {
     P.kernel = kGeneric;
     P.row_chunk = P.rows < kMaxRowChunk ? P.rows : kMaxRowChunk;
@@ -130,8 +130,9 @@ extern "C" int fp8kv_attn_plan(const fp8kv_attn_desc* d, fp8kv_attn_plan_t* plan
 
   // Split count: about one wave of CTAs (two for the generic path), never
   // more partitions than tiles of work (dense: tokens / tile, sparse: entries
-  // / (tile / 4)), and partitions capped in length because FP32 accumulation
-  // error grows with the number of tiles one partition sums.
+  // / (tile / 4)), and partitions capped in length where FP32 accumulation
+  // error grows with the number of tiles one partition sums (the query-row
+  // and CUDA-core kernels; the small-group kernel's cap is far longer).
   const int64_t units = (int64_t)d->batch * d->num_kv_heads * n_chunks;
   const int max_tiles = d->mode == FP8KV_MODE_DENSE
                             ? (d->max_kv_len > 0 ? ceil_div(d->max_kv_len, tile) : 1)

@@ -7,6 +7,15 @@
 
 namespace fp8kv {
 
+// tok / page_size for 0 <= tok < 2^31, given page_div = ceil(2^64 /
+// page_size) (0 for page size 1): the high word of one 64-bit multiply
+// instead of an integer division, whose long dependent instruction sequence
+// is costly on the copy-issuing threads (exact for every numerator below
+// 2^32: Lemire, Kaser and Kurz, "Faster remainder by direct computation").
+__device__ __forceinline__ int div_page(int tok, int page_size, unsigned long long page_div) {
+  return page_size == 1 ? tok : (int)__umul64hi(page_div, (unsigned long long)(unsigned)tok);
+}
+
 // log2(e): logits are kept in base-2 units so that softmax uses exp2.
 constexpr float kLog2e = 1.4426950408889634f;
 

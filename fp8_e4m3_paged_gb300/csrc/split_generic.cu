@@ -203,8 +203,9 @@ __global__ void __launch_bounds__(NT) split_generic(Params p) {
       if (MODE == FP8KV_MODE_DENSE) {
         const int tok = tb + t;
         if (tok < u1) {
-          const int blk = p.block_table[(int64_t)b * p.bt_stride + tok / p.page_size];
-          const int slot = tok % p.page_size;
+          const int page = div_page(tok, p.page_size, p.page_div);
+          const int blk = p.block_table[(int64_t)b * p.bt_stride + page];
+          const int slot = tok - page * p.page_size;
           if (blk >= 0 && blk < p.num_kv_blocks) {
             ok = true;
             kp = p.k_cache + blk * p.ksb + slot * p.kst + g * p.ksh;

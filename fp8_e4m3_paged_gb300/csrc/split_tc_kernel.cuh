@@ -342,12 +342,8 @@ struct TilePages {
   int bid;  // this lane's page
 };
 
-// The page of token `tok` (0 <= tok < 2^31): a multiply-high by the host's
-// rounded-up reciprocal instead of an integer division, whose long dependent
-// sequence paced the producer loop.
-__device__ __forceinline__ int page_of(const Params& p, int tok) {
-  return p.page_size == 1 ? tok : (int)__umul64hi(p.page_div, (unsigned long long)(unsigned)tok);
-}
+// The page of token `tok` (0 <= tok < 2^31).
+__device__ __forceinline__ int page_of(const Params& p, int tok) { return div_page(tok, p.page_size, p.page_div); }
 
 __device__ __forceinline__ TilePages fetch_pages(const Params& p, int b, int u0, int u1, int i, int lane) {
   TilePages tp;

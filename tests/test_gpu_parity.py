@@ -110,9 +110,9 @@ def test_c4_full(kernel, floor_elements):
     except at most `floor_elements`, which must lie within the FP32-state
     floor of tests/_check.py (value and logit terms).  Measured: CUDA-core
     kernel one element, (0, 0, 7, 70) at 4.45 ulps, |out| 6000x below its
-    cond; small-group kernel two, (2, 0, 18, 127) at 4.06 ulps (cancellation
-    4900x) and (57, 0, 11, 0) at 5.25 ulps (cancellation 133000x); each within
-    0.4 % of its floor bound."""
+    cond; small-group kernel (6 partitions per request) two, the worst
+    (57, 0, 11, 0) at 5.25 ulps (cancellation 133000x); no element uses more
+    than 13 % of its bound."""
     p = _problem("c4")
     dp = _dp(p, kernel=kernel)
     if kernel == 0:
