@@ -75,6 +75,23 @@ def test_plan_split_override_and_batch0(B):
     assert p0.workspace_bytes >= 4
 
 
+@pytest.mark.parametrize("kernel,cap", [(3, 128), (2, 32), (1, None)])
+def test_plan_partition_length_cap(B, kernel, cap):
+    """A batch with more (request, KV head) units than SMs is split by
+    length: the longest request's partitions hold at most `cap` tiles of 64
+    tokens (the small-group kernel drains each pair of tiles into a
+    compensated sum, so its cap is four times the others')."""
+    L = 46000
+    p = B.fp8kv_attn_plan(_desc(B, batch=64, q_max=1, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                                max_kv_len=L, max_blocks=(L + 15) // 16, num_kv_blocks=4608, kernel=kernel))
+    assert p.kernel == kernel
+    if cap is None:
+        return
+    tiles = -(-L // 64)
+    assert p.num_splits == -(-tiles // cap)
+    assert p.min_part == 16 * 64
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=96), -2),
     (dict(q_max=17), -2),
