@@ -182,11 +182,11 @@ def test_shapes_dense(D, q, Hq, Hkv):
 
 
 @pytest.mark.parametrize("page_size", [1, 2, 3, 64, 97, 1000, 4099])
-@pytest.mark.parametrize("kernel", [2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_page_sizes(page_size, kernel):
-    """Token -> (page, slot) on the tensor-core kernels, which divide by the
-    page size with a multiply-high: page size 1 (its own branch), powers of
-    two, odd sizes, and pages longer than a whole partition."""
+    """Token -> (page, slot) on every split kernel, each of which divides by
+    the page size with a multiply-high: page size 1 (its own branch), powers
+    of two, odd sizes, and pages longer than a whole partition."""
     p = make_dense(B=2, q=2, Hq=8, Hkv=2, D=128, page_size=page_size, lens=[700, 1333],
                    seed=900 + page_size + kernel)
     dp = _dp(p, kernel=kernel)
